@@ -1,0 +1,380 @@
+#!/usr/bin/env python
+"""Benchmark of the absorbed-form MLA split-KV decode on GB300.
+
+One step = one ``mla_decode`` call (decode kernel + split-K combine) over one batch of the
+chosen workload, with every input resident in HBM.  Prints ONE JSON line (rank 0):
+KV-cache GB/s (the value), microseconds per call, TFLOP/s, the roofline fraction of the
+path against the measured HBM / bf16 peaks, an end-to-end figure through the C ABI with
+host buffers, the float64 CPU oracle timed on a bounded sample, and the SM clocks seen.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+For N > 1 it is launched by torch.distributed.run, one rank per GPU; every rank decodes
+its own copy of the workload (independent replicas, weak scaling) and the slowest rank's
+time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLA decode µs/call, KV-cache GB/s and % of roofline on 1 GB300"
+DEFAULT_WORKLOAD = "paged_bf16_uniform"
+BYTES_PER_TOKEN = {"bf16": 1152, "fp8": 576, "nvfp4": 324}
+L2_FLUSH_BYTES = 512 << 20  # > 4x the 129 MB L2
+
+
+def algorithmic_work(inp) -> tuple[float, float, float]:
+    """(bytes, flops, kv_bytes) one decode call must move / compute at minimum: the cache
+    rows of every visible position once, the queries, outputs, LSEs, the block-table
+    entries read and seq_lens; FLOPs of QK^T (576) and PV (512) per visible position."""
+    import numpy as np
+    w = inp["workload"]
+    sl = np.clip(inp["seq_lens"].astype(np.int64), 0, None)
+    T = int(sl.sum())
+    kv = T * BYTES_PER_TOKEN[w.kv_dtype]
+    io = w.B * w.q_len * w.H * (576 * 2 + 512 * 2 + 4)
+    table = int(sum(-(-int(L) // w.page_size) for L in sl)) * 4 + 4 * w.B
+    vis = sum(max(0, int(L) - w.q_len + i + 1) for L in sl for i in range(w.q_len))
+    flops = 2.0 * w.H * (576 + 512) * vis
+    return float(kv + io + table), flops, float(kv)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mla_latent_kv_split_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, fn), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(workload: str):
+    """ncu DRAM bytes per decode launch for this workload, if recorded for the current
+    kernel sources (profiles/traffic.json); None otherwise."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(workload)
+    if not d or d.get("source_sha") != kernel_source_sha():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason samples while the GPU works."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=lambda: [self.lines.append(l) for l in self.proc.stdout], daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        if self.proc is None:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["nvidia-smi unavailable"], samples=0)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return dict(sm_mhz=statistics.median(sm) if sm else None, sm_max_mhz=max(mx) if mx else None,
+                    reasons=sorted(reasons), samples=len(sm))
+
+
+def cpu_oracle_sample(inp, seconds: float, start_b: int = 0):
+    """The float64 oracle, as it stands, on whole requests of the workload until `seconds`
+    of CPU time have passed.  Returns (kv_bytes, elapsed, requests, rows)."""
+    import oracle
+    w = inp["workload"]
+    kv_b, n_req, rows = 0.0, 0, 0
+    t0 = time.perf_counter()
+    b = start_b
+    while True:
+        bb = b % w.B
+        oracle.mla_decode_ref(inp["q_nope"], inp["q_pe"], inp["cache"], inp["block_table"], inp["seq_lens"],
+                              w.sm_scale, kv_dtype=w.kv_dtype, kv_scale=inp["kv_scale"], page_size=w.page_size,
+                              rows=[(bb, i) for i in range(w.q_len)])
+        kv_b += max(0, int(inp["seq_lens"][bb])) * BYTES_PER_TOKEN[w.kv_dtype]
+        n_req += 1
+        rows += w.q_len
+        b += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or n_req >= 4 * w.B:
+            return kv_b, el, n_req, rows
+
+
+def cores_used() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def workload_config(w, l2_note: str):
+    cfg = {"workload": w.name, "B": w.B, "q_len": w.q_len, "H": w.H, "page_size": w.page_size,
+           "kv_dtype": w.kv_dtype, "sm_scale": "1/sqrt(192)", "num_splits": w.num_splits or "schedule",
+           "l2": l2_note}
+    if w.seq_len is not None:
+        cfg["seq_len"] = w.seq_len
+    if w.ragged is not None:
+        cfg["seq_lens"] = f"uniform integers in [{w.ragged[0]}, {w.ragged[1]}], seed {w.seed}"
+    return cfg
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return world, rank, local
+
+
+def run_reference(args):
+    """The float64 CPU oracle, timed on this host's cores, on bounded samples of the same
+    workload: one request per step."""
+    world, rank, _ = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0
+    if rank != 0:
+        return
+    from mla_latent_kv_split_gb300 import workloads as W
+    w = W.WORKLOADS[args.workload]
+    inp = W.make_inputs(w)
+    for s in range(args.warmup):
+        cpu_oracle_sample(inp, 0.0, start_b=s)
+    t_steps, kv_total, rows_total = [], 0.0, 0
+    for s in range(args.steps):
+        kv_b, el, n_req, rows = cpu_oracle_sample(inp, 0.0, start_b=args.warmup + s)
+        t_steps.append(el)
+        kv_total += kv_b
+        rows_total += rows
+    total = sum(t_steps)
+    value = kv_total / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, "n/a (CPU)"),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores_used(), "kind": "oracle",
+                         "sample": f"one whole request (all {w.q_len} queries, {w.H} heads) per step, "
+                                   f"{args.steps} steps, {rows_total} (b,i) rows"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    world, rank, local = dist_setup(args.gpus)
+    from mla_latent_kv_split_gb300 import binding as mb
+    from mla_latent_kv_split_gb300 import build
+    from mla_latent_kv_split_gb300 import workloads as W
+
+    if rank == 0:
+        build.build()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = W.WORKLOADS[args.workload]
+    inp = W.make_inputs(w)
+    nbytes, flops, kv_bytes = algorithmic_work(inp)
+
+    def to_dev(a, bf16=False):
+        t = torch.from_numpy(a.view(np.int16) if bf16 else a)
+        return (t.view(torch.bfloat16) if bf16 else t).to(dev)
+
+    q_nope = to_dev(inp["q_nope"], True)
+    q_pe = to_dev(inp["q_pe"], True)
+    cache = to_dev(inp["cache"], inp["cache"].dtype == np.uint16)
+    table = to_dev(inp["block_table"])
+    seq_lens = to_dev(inp["seq_lens"])
+    ws = mb.alloc_workspace(w.B, w.q_len, w.H, w.num_splits, dev)
+    out = torch.empty((w.B, w.q_len, w.H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.q_len, w.H), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        mb.mla_decode(q_nope, q_pe, cache, table, seq_lens, w.sm_scale, w.kv_dtype, inp["kv_scale"],
+                      w.num_splits, page_size=w.page_size, num_pages=inp["num_pages"], workspace=ws, out=out,
+                      lse=lse, stream=stream)
+
+    sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    sampler.start()
+    t_warm = time.perf_counter()
+    k = 0
+    while k < max(3, args.warmup) or time.perf_counter() - t_warm < 0.3:
+        flush.zero_()
+        call()
+        torch.cuda.synchronize()
+        k += 1
+    status = mb.mla_decode_read_status(ws)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for s in range(args.steps):
+        flush.zero_()
+        evs[s][0].record(stream)
+        call()
+        evs[s][1].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    times_ms = [a.elapsed_time(b) for a, b in evs]
+    clocks = sampler.stop()
+    t_mean = sum(times_ms) / len(times_ms)
+
+    # end to end through the C ABI with host buffers: inputs copied in, results copied out
+    pin = lambda a: torch.from_numpy(a).pin_memory()
+    h_qn, h_qp, h_bt, h_sl = pin(inp["q_nope"].view(np.int16)), pin(inp["q_pe"].view(np.int16)), \
+        pin(inp["block_table"]), pin(inp["seq_lens"])
+    h_out = torch.empty((w.B, w.q_len, w.H, 512), dtype=torch.int16).pin_memory()
+    h_lse = torch.empty((w.B, w.q_len, w.H), dtype=torch.float32).pin_memory()
+    d_qn, d_qp = torch.empty_like(h_qn, device=dev), torch.empty_like(h_qp, device=dev)
+    d_bt, d_sl = torch.empty_like(h_bt, device=dev), torch.empty_like(h_sl, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in (h_qn, h_qp, h_bt, h_sl))
+    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+    e2e_ms = []
+    for s in range(args.warmup + args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        d_qn.copy_(h_qn, non_blocking=True)
+        d_qp.copy_(h_qp, non_blocking=True)
+        d_bt.copy_(h_bt, non_blocking=True)
+        d_sl.copy_(h_sl, non_blocking=True)
+        mb.mla_decode(d_qn.view(torch.bfloat16), d_qp.view(torch.bfloat16), cache, d_bt, d_sl, w.sm_scale,
+                      w.kv_dtype, inp["kv_scale"], w.num_splits, page_size=w.page_size,
+                      num_pages=inp["num_pages"], workspace=ws, out=out, lse=lse, stream=stream)
+        h_out.copy_(out.view(torch.int16), non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if s >= args.warmup:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e_mean = sum(e2e_ms) / len(e2e_ms)
+
+    if world > 1:
+        t = torch.tensor([t_mean, e2e_mean], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_mean, e2e_mean = float(t[0]), float(t[1])
+    if rank != 0:
+        dist.destroy_process_group()
+        return
+
+    peaks = load_peaks()
+    t_s = t_mean * 1e-3
+    t_mem = nbytes / (peaks["hbm"] * 1e9)
+    t_mma = flops / (peaks["bf16"] * 1e12)
+    if t_mem >= t_mma:
+        roof = {"bound": "hbm", "achieved": nbytes / t_s / 1e9, "peak": peaks["hbm"], "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": flops / t_s / 1e12, "peak": peaks["bf16"], "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = traffic_for(w.name)
+    roof["peak_source"] = peaks["source"]
+    roof["roofline_us"] = 1e6 * max(t_mem, t_mma)
+    roof["kernel"] = "mla_decode call (decode kernel + split-K combine)"
+
+    cpu_kv, cpu_el, cpu_req, cpu_rows = cpu_oracle_sample(inp, args.cpu_seconds)
+    line = {
+        "metric": METRIC, "value": world * kv_bytes / t_s / 1e9, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_mean, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(w, "flushed between steps (512 MB write)"),
+        "us_per_call": 1e3 * t_mean, "us_per_call_median": 1e3 * statistics.median(times_ms),
+        "kv_gbs": kv_bytes / t_s / 1e9, "tflops": flops / t_s / 1e12,
+        "algorithmic_bytes": nbytes, "algorithmic_flops": flops, "device_status": status,
+        "roofline": roof,
+        "cpu_baseline": {"value": cpu_kv / cpu_el / 1e9, "unit": "GB/s", "cores": cores_used(), "kind": "oracle",
+                         "sample": f"{cpu_req} whole requests ({cpu_rows} (b,i) rows x {w.H} heads) of the same "
+                                   f"workload, {cpu_el:.1f} s, float64 NumPy"},
+        "e2e": {"value": world * kv_bytes / (e2e_mean * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_mean,
+                "note": "q_nope, q_pe, block_table, seq_lens copied in from pinned host memory and out, lse "
+                        "copied back every step; the KV cache is resident device state"},
+        "clocks": clocks,
+        "gpu_launches": 2 * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

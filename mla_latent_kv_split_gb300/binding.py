@@ -1,0 +1,169 @@
+"""Python binding of ``libmla_decode.so`` (the C ABI in ``include/mla_decode.h``).
+
+Argument marshalling only: shapes and raw device pointers are read from torch tensors
+(torch is used for device memory and streams) and passed to the C entry points of the
+same names.  Every step of the decode runs in the library's CUDA kernels; there is no
+fallback of any kind, and a missing library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libmla_decode.so")
+
+MLA_KV_BF16, MLA_KV_FP8_E4M3, MLA_KV_NVFP4 = 0, 1, 2
+KV_DTYPE = {"bf16": MLA_KV_BF16, "fp8": MLA_KV_FP8_E4M3, "nvfp4": MLA_KV_NVFP4}
+STATUS_BITS = {
+    0x1: "PAGE_OUT_OF_RANGE", 0x2: "SEQ_TOO_LONG", 0x4: "SEQ_LT_QLEN", 0x8: "NEG_SEQ_LEN",
+    0x10: "WAIT_TIMEOUT", 0x20: "Q_RANGE",
+}
+EXPORTED = (
+    "mla_decode_abi_version", "mla_status_string", "mla_decode_workspace_size", "mla_decode",
+    "mla_splitk_reduce", "mla_decode_read_status", "mla_decode_num_workers", "mla_decode_plan_host",
+)
+
+
+class MLAError(RuntimeError):
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__(f"{fn} failed: {msg} ({code})")
+        self.code = code
+
+
+_lock = threading.Lock()
+_handle = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (opened once).  Raises if it has not been built."""
+    global _handle
+    with _lock:
+        if _handle is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                                   "or python mla_latent_kv_split_gb300/build.py")
+            h = ctypes.CDLL(LIB_PATH)
+            P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+            h.mla_decode_abi_version.restype = I
+            h.mla_status_string.restype = ctypes.c_char_p
+            h.mla_status_string.argtypes = [I]
+            h.mla_decode_workspace_size.restype = I
+            h.mla_decode_workspace_size.argtypes = [I, I, I, I, ctypes.POINTER(Z)]
+            h.mla_decode.restype = I
+            h.mla_decode.argtypes = [P, P, P, P, I, P, I, I, I, I, I, F, I, F, I, P, Z, P, P, P]
+            h.mla_splitk_reduce.restype = I
+            h.mla_splitk_reduce.argtypes = [P, Z, I, I, I, P, P, P]
+            h.mla_decode_read_status.restype = I
+            h.mla_decode_read_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
+            h.mla_decode_num_workers.restype = I
+            h.mla_decode_num_workers.argtypes = [ctypes.POINTER(I)]
+            i32p = ctypes.POINTER(ctypes.c_int32)
+            h.mla_decode_plan_host.restype = I
+            h.mla_decode_plan_host.argtypes = [i32p, I, I, I, I, I, I, i32p, i32p, i32p, i32p, i32p]
+            _handle = h
+        return _handle
+
+
+def _check(fn: str, code: int) -> None:
+    if code != 0:
+        raise MLAError(fn, code, lib().mla_status_string(code).decode())
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream_ptr(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def mla_decode_workspace_size(B: int, q_len: int, H: int, num_splits: int = 0) -> int:
+    n = ctypes.c_size_t(0)
+    _check("mla_decode_workspace_size", lib().mla_decode_workspace_size(B, q_len, H, num_splits, ctypes.byref(n)))
+    return n.value
+
+
+def mla_decode_num_workers() -> int:
+    w = ctypes.c_int(0)
+    _check("mla_decode_num_workers", lib().mla_decode_num_workers(ctypes.byref(w)))
+    return w.value
+
+
+def alloc_workspace(B: int, q_len: int, H: int, num_splits: int = 0, device=None):
+    """A torch uint8 device buffer of the size mla_decode needs (plumbing only)."""
+    import torch
+    n = mla_decode_workspace_size(B, q_len, H, num_splits)
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def mla_decode(q_nope, q_pe, kv_cache, block_table, seq_lens, sm_scale: float, kv_dtype="bf16",
+               kv_scale: float = 1.0, num_splits: int = 0, page_size: int | None = None,
+               num_pages: int | None = None, workspace=None, out=None, lse=None, stream=None):
+    """Calls ``mla_decode``.  Tensors: ``q_nope [B,q_len,H,512]`` / ``q_pe [B,q_len,H,64]``
+    bf16, ``kv_cache`` (``[P,ps,576]`` bf16 / uint8, or ``[P, ps*324]`` uint8 for NVFP4 with
+    ``page_size`` given), ``block_table [B,max_pages]`` int32, ``seq_lens [B]`` int32, all on
+    the device.  Returns ``(out, lse)`` (allocated with torch when not given)."""
+    import torch
+    B, q_len, H, _ = q_nope.shape
+    kd = KV_DTYPE[kv_dtype] if isinstance(kv_dtype, str) else int(kv_dtype)
+    if page_size is None:
+        page_size = kv_cache.shape[1]
+    if num_pages is None:
+        num_pages = kv_cache.shape[0]
+    if workspace is None:
+        workspace = alloc_workspace(B, q_len, H, num_splits, q_nope.device)
+    if out is None:
+        out = torch.empty((B, q_len, H, 512), dtype=torch.bfloat16, device=q_nope.device)
+    if lse is None:
+        lse = torch.empty((B, q_len, H), dtype=torch.float32, device=q_nope.device)
+    nbytes = workspace.numel() * workspace.element_size() if not isinstance(workspace, int) else 1 << 62
+    _check("mla_decode", lib().mla_decode(
+        _ptr(q_nope), _ptr(q_pe), _ptr(kv_cache), _ptr(block_table), int(block_table.shape[1]),
+        _ptr(seq_lens), B, q_len, H, int(num_pages), int(page_size), float(sm_scale), kd,
+        float(kv_scale), int(num_splits), _ptr(workspace), nbytes, _ptr(out), _ptr(lse),
+        _stream_ptr(stream)))
+    return out, lse
+
+
+def mla_splitk_reduce(workspace, B: int, q_len: int, H: int, out, lse=None, stream=None):
+    _check("mla_splitk_reduce", lib().mla_splitk_reduce(
+        _ptr(workspace), workspace.numel() * workspace.element_size(), B, q_len, H, _ptr(out), _ptr(lse),
+        _stream_ptr(stream)))
+    return out, lse
+
+
+def mla_decode_read_status(workspace, stream=None) -> int:
+    """The device status word of the last decode on ``workspace`` (synchronises)."""
+    v = ctypes.c_uint32(0)
+    code = lib().mla_decode_read_status(_ptr(workspace), ctypes.byref(v), _stream_ptr(stream))
+    if code not in (0, 5):
+        _check("mla_decode_read_status", code)
+    return v.value
+
+
+def mla_decode_plan_host(seq_lens, q_len: int, max_pages: int, page_size: int, num_splits: int = 0,
+                         workers: int = 0):
+    """The schedule as the kernels evaluate it, computed on the host (for tests)."""
+    sl = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+    B = sl.shape[0]
+    U = B * q_len
+    arrs = [np.zeros(U, dtype=np.int32) for _ in range(4)]
+    used = ctypes.c_int32(0)
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    _check("mla_decode_plan_host", lib().mla_decode_plan_host(
+        sl.ctypes.data_as(i32p), B, q_len, max_pages, page_size, num_splits, workers,
+        *[a.ctypes.data_as(i32p) for a in arrs], ctypes.byref(used)))
+    return dict(tile_begin=arrs[0], tiles=arrs[1], parts=arrs[2], slot=arrs[3], slots_used=used.value)

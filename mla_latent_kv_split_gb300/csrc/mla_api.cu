@@ -1,0 +1,213 @@
+// mla_api.cu -- the C ABI (include/mla_decode.h): host-side validation, workspace sizing,
+// the host copy of the schedule, and the launches.  Everything is enqueued on the
+// caller's stream; nothing here allocates device memory or synchronises, except
+// mla_decode_read_status.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+#include <vector>
+
+#include "mla_device.cuh"
+
+#define MLA_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace mla {
+cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_splitk_reduce(const uint8_t* ws, int U, int H, int slots_cap, uint16_t* out,
+                                 float* lse, cudaStream_t stream, bool pdl);
+}  // namespace mla
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int g_workers[kMaxDevices] = {0};
+
+// Scheduling workers on the current device: one per pair of SMs.
+cudaError_t current_workers(int* workers) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_workers[dev] == 0) {
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    g_workers[dev] = sms >= 2 ? sms / 2 : 1;
+  }
+  *workers = g_workers[dev];
+  return cudaSuccess;
+}
+
+bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
+
+mla_status_t check_shape(int B, int q_len, int H, int num_splits) {
+  if (B < 0 || q_len < 1 || H < 1 || num_splits < 0) return MLA_ERR_INVALID_ARG;
+  if (H % 16 != 0 || H > MLA_MAX_HEADS) return MLA_ERR_UNSUPPORTED;
+  if (q_len > MLA_MAX_Q_LEN) return MLA_ERR_UNSUPPORTED;
+  if ((long long)B * q_len > MLA_MAX_UNITS) return MLA_ERR_UNSUPPORTED;
+  if (num_splits > 4096) return MLA_ERR_UNSUPPORTED;
+  return MLA_OK;
+}
+
+mla_status_t check_geometry(int B, int q_len, int max_pages, int num_pages, int page_size) {
+  if (max_pages < 1 || num_pages < 1) return MLA_ERR_INVALID_ARG;
+  if (page_size != 32 && page_size != 64) return MLA_ERR_UNSUPPORTED;
+  if ((long long)max_pages * page_size > 0x7fffffffLL) return MLA_ERR_UNSUPPORTED;
+  if ((long long)B * q_len * max_pages > 0x7fffffffLL) return MLA_ERR_UNSUPPORTED;
+  return MLA_OK;
+}
+
+size_t required_bytes(int units, int H, int num_splits, int workers) {
+  return mla::workspace_bytes_for(mla::max_slots(units, num_splits, workers), H);
+}
+
+int slots_that_fit(size_t workspace_bytes, int H) {
+  if (workspace_bytes < mla::kHeaderBytes) return 0;
+  size_t per = (size_t)H * (mla::kLatent + 1) * 4;
+  size_t n = (workspace_bytes - mla::kHeaderBytes) / per;
+  return n > 0x7fffffff ? 0x7fffffff : (int)n;
+}
+
+}  // namespace
+
+MLA_EXPORT int mla_decode_abi_version(void) { return 1; }
+
+MLA_EXPORT const char* mla_status_string(mla_status_t s) {
+  switch (s) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+    case MLA_ERR_WORKSPACE_TOO_SMALL: return "MLA_ERR_WORKSPACE_TOO_SMALL";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    case MLA_ERR_DEVICE_STATUS: return "MLA_ERR_DEVICE_STATUS";
+  }
+  return "MLA_ERR_UNKNOWN";
+}
+
+MLA_EXPORT mla_status_t mla_decode_num_workers(int* workers) {
+  if (!workers) return MLA_ERR_INVALID_ARG;
+  return current_workers(workers) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+MLA_EXPORT mla_status_t mla_decode_workspace_size(int B, int q_len, int H, int num_splits,
+                                                  size_t* bytes) {
+  if (!bytes || B < 1) return MLA_ERR_INVALID_ARG;
+  mla_status_t st = check_shape(B, q_len, H, num_splits);
+  if (st != MLA_OK) return st;
+  int C = 0;
+  if (current_workers(&C) != cudaSuccess) return MLA_ERR_CUDA;
+  *bytes = required_bytes(B * q_len, H, num_splits, C);
+  return MLA_OK;
+}
+
+MLA_EXPORT mla_status_t mla_decode_plan_host(const int32_t* seq_lens, int B, int q_len, int max_pages,
+                                             int page_size, int num_splits, int workers,
+                                             int32_t* unit_tile_begin, int32_t* unit_tiles,
+                                             int32_t* unit_parts, int32_t* unit_slot,
+                                             int32_t* slots_used) {
+  if (!seq_lens || !unit_tile_begin || !unit_tiles || !unit_parts || !unit_slot || !slots_used)
+    return MLA_ERR_INVALID_ARG;
+  if (B < 1) return MLA_ERR_INVALID_ARG;
+  mla_status_t st = check_shape(B, q_len, 16, num_splits);
+  if (st != MLA_OK) return st;
+  st = check_geometry(B, q_len, max_pages, 1, page_size);
+  if (st != MLA_OK) return st;
+  int C = workers;
+  if (C <= 0 && current_workers(&C) != cudaSuccess) return MLA_ERR_CUDA;
+  std::vector<mla::UnitPlan> plan((size_t)B * q_len);
+  int slots = mla::plan_host(seq_lens, B, q_len, max_pages, page_size, num_splits, C, plan.data());
+  for (int u = 0; u < B * q_len; ++u) {
+    unit_tile_begin[u] = plan[u].tile_begin;
+    unit_tiles[u] = plan[u].tiles;
+    unit_parts[u] = plan[u].parts;
+    unit_slot[u] = plan[u].slot;
+  }
+  *slots_used = slots;
+  return MLA_OK;
+}
+
+MLA_EXPORT mla_status_t mla_decode(const void* q_nope, const void* q_pe, const void* kv_cache,
+                                   const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                                   int B, int q_len, int H, int num_pages, int page_size, float sm_scale,
+                                   int kv_dtype, float kv_scale, int num_splits, void* workspace,
+                                   size_t workspace_bytes, void* out, float* lse, mla_stream_t stream) {
+  mla_status_t st = check_shape(B, q_len, H, num_splits);
+  if (st != MLA_OK) return st;
+  st = check_geometry(B, q_len, max_pages, num_pages, page_size);
+  if (st != MLA_OK) return st;
+  if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3 && kv_dtype != MLA_KV_NVFP4)
+    return MLA_ERR_INVALID_ARG;
+  if (!isfinite(sm_scale)) return MLA_ERR_INVALID_ARG;
+  if (kv_dtype == MLA_KV_FP8_E4M3 && !(isfinite(kv_scale) && kv_scale > 0.f)) return MLA_ERR_INVALID_ARG;
+  if (B == 0) return MLA_OK;
+  if (!q_nope || !q_pe || !kv_cache || !block_table || !seq_lens || !workspace || !out)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned(q_nope, 16) || !aligned(q_pe, 16) || !aligned(kv_cache, 128) || !aligned(block_table, 16) ||
+      !aligned(seq_lens, 4) || !aligned(workspace, 256) || !aligned(out, 16) || (lse && !aligned(lse, 4)))
+    return MLA_ERR_INVALID_ARG;
+  int C = 0;
+  if (current_workers(&C) != cudaSuccess) return MLA_ERR_CUDA;
+  const int U = B * q_len;
+  if (workspace_bytes < required_bytes(U, H, num_splits, C)) return MLA_ERR_WORKSPACE_TOO_SMALL;
+
+  mla::DecodeParams p;
+  p.q_nope = static_cast<const uint16_t*>(q_nope);
+  p.q_pe = static_cast<const uint16_t*>(q_pe);
+  p.cache = static_cast<const uint8_t*>(kv_cache);
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.max_pages = max_pages;
+  p.B = B;
+  p.q_len = q_len;
+  p.H = H;
+  p.num_pages = num_pages;
+  p.page_size = page_size;
+  p.sm_scale = sm_scale;
+  p.kv_scale = kv_dtype == MLA_KV_FP8_E4M3 ? kv_scale : 1.f;
+  p.kv_dtype = kv_dtype;
+  p.num_splits = num_splits;
+  p.workers = C;
+  p.slots_cap = slots_that_fit(workspace_bytes, H);
+  p.ws = static_cast<uint8_t*>(workspace);
+  p.out = static_cast<uint16_t*>(out);
+  p.lse = lse;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, 16, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (mla::launch_decode_simt(p, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (mla::launch_splitk_reduce(p.ws, U, H, p.slots_cap, p.out, lse, s, true) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+MLA_EXPORT mla_status_t mla_splitk_reduce(const void* workspace, size_t workspace_bytes, int B, int q_len,
+                                          int H, void* out, float* lse, mla_stream_t stream) {
+  mla_status_t st = check_shape(B, q_len, H, 0);
+  if (st != MLA_OK) return st;
+  if (B == 0) return MLA_OK;
+  if (!workspace || !out) return MLA_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256) || !aligned(out, 16) || (lse && !aligned(lse, 4))) return MLA_ERR_INVALID_ARG;
+  if (workspace_bytes < mla::kHeaderBytes) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (mla::launch_splitk_reduce(static_cast<const uint8_t*>(workspace), B * q_len, H,
+                                slots_that_fit(workspace_bytes, H), static_cast<uint16_t*>(out), lse, s,
+                                false) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+MLA_EXPORT mla_status_t mla_decode_read_status(const void* workspace, uint32_t* device_status,
+                                               mla_stream_t stream) {
+  if (!workspace || !device_status) return MLA_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  if (cudaMemcpyAsync(&v, workspace, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MLA_ERR_CUDA;
+  *device_status = v;
+  return v ? MLA_ERR_DEVICE_STATUS : MLA_OK;
+}

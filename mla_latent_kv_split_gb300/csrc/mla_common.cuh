@@ -1,0 +1,137 @@
+// mla_common.cuh -- constants, the split schedule and the workspace layout shared by the
+// host layer and every kernel of the MLA split-KV decode.
+//
+// The schedule (which scheduling worker covers which KV range of which (b, i)) is a pure
+// function of seq_lens, q_len, the page geometry, num_splits and the worker count.  The
+// kernels evaluate it on the device from seq_lens (no host sync, graph-safe); the host
+// evaluates the same inline functions only to answer mla_decode_plan_host for tests.
+#pragma once
+
+#include <stdint.h>
+
+#include "../../include/mla_decode.h"
+
+#if defined(__CUDACC__)
+#define MLA_HD __host__ __device__ __forceinline__
+#else
+#define MLA_HD inline
+#endif
+
+namespace mla {
+
+constexpr int kLatent = MLA_LATENT_DIM;  // 512: latent, also V
+constexpr int kRope = MLA_ROPE_DIM;      // 64
+constexpr int kDim = MLA_CACHE_DIM;      // 576
+constexpr int kTile = 64;                // tokens per schedule tile
+constexpr int kMaxUnits = MLA_MAX_UNITS; // B * q_len
+constexpr int kNvfp4Group = 16;
+
+// Workspace layout (bytes):
+//   [0, 4)                      device status word (reset by the host each call)
+//   [4, 8)                      schedule mode written by the decode kernel
+//   [kPlanOffset, +8*units)     plan: per unit {parts, first partial slot}
+//   [kHeaderBytes, ...)         partial outputs  fp32 [slots][H][512]
+//   then                        partial LSEs     fp32 [slots][H]
+constexpr size_t kPlanOffset = 256;
+constexpr size_t kHeaderBytes = 32768;
+static_assert(kPlanOffset + 8 * (size_t)kMaxUnits <= kHeaderBytes, "plan must fit the header");
+
+MLA_HD size_t partial_o_offset() { return kHeaderBytes; }
+MLA_HD size_t partial_lse_offset(int slots, int H) {
+  return kHeaderBytes + (size_t)slots * H * kLatent * 4;
+}
+MLA_HD size_t workspace_bytes_for(int slots, int H) {
+  return kHeaderBytes + (size_t)slots * H * (kLatent + 1) * 4;
+}
+
+MLA_HD int cdiv_i(int a, int b) { return (a + b - 1) / b; }
+
+// Positions query i of q_len may see: t < seq_len - q_len + i + 1 (the last q_len cache
+// positions are this step's tokens); seq_len is clamped to [0, max_pages*page_size].
+MLA_HD int clamp_seq_len(int seq_len, int max_pages, int page_size) {
+  long long cap = (long long)max_pages * page_size;
+  if (seq_len < 0) return 0;
+  return (long long)seq_len > cap ? (int)cap : seq_len;
+}
+MLA_HD int unit_visible(int seq_len_clamped, int q_len, int i) {
+  int v = seq_len_clamped - q_len + i + 1;
+  return v < 0 ? 0 : v;
+}
+
+// ---- heuristic mode (num_splits == 0): contiguous, balanced tile ranges per worker ----
+// With N tiles and C workers, only C' = min(C, N) workers get work, so no range is empty;
+// worker c < C' owns global tiles [floor(c*N/C'), floor((c+1)*N/C')).  Callers pass C'.
+MLA_HD int active_workers(long long N, int C) { return N < (long long)C ? (int)N : C; }
+MLA_HD long long worker_begin(int c, long long N, int C) { return (long long)c * N / C; }
+// The worker whose range holds tile t (0 <= t < N): the largest c with begin(c) <= t.
+MLA_HD int worker_of(long long t, long long N, int C) {
+  return (int)(((t + 1) * (long long)C + N - 1) / N - 1);
+}
+
+// ---- forced mode (num_splits > 0): each unit cut into ranges of span tiles ----
+MLA_HD int forced_span_tiles(int visible, int num_splits) {
+  if (visible <= 0) return 1;
+  int span_tok = cdiv_i(visible, num_splits);
+  return cdiv_i(span_tok, kTile);
+}
+
+// One unit's share of the schedule.
+struct UnitPlan {
+  int tile_begin;  // heuristic: first global tile; forced: first global item
+  int tiles;       // tiles of visible KV
+  int parts;       // number of KV ranges it is cut into (0 when nothing is visible)
+  int slot;        // first partial slot, -1 when written directly (parts <= 1)
+};
+
+// Host evaluation of the whole plan (the device kernels evaluate the same formulas with a
+// block-wide scan).  Returns the number of partial slots used.
+inline int plan_host(const int32_t* seq_lens, int B, int q_len, int max_pages, int page_size,
+                     int num_splits, int C, UnitPlan* plan) {
+  const int U = B * q_len;
+  long long N = 0;
+  for (int u = 0; u < U; ++u) {
+    int b = u / q_len, i = u % q_len;
+    int L = clamp_seq_len(seq_lens[b], max_pages, page_size);
+    int vis = unit_visible(L, q_len, i);
+    plan[u].tiles = cdiv_i(vis, kTile);
+    if (num_splits > 0) {
+      plan[u].parts = plan[u].tiles ? cdiv_i(plan[u].tiles, forced_span_tiles(vis, num_splits)) : 0;
+      plan[u].tile_begin = (int)N;  // first item index
+      N += plan[u].parts;
+    } else {
+      plan[u].tile_begin = (int)N;
+      N += plan[u].tiles;
+    }
+  }
+  int slots = 0;
+  const int Ca = active_workers(N, C);
+  for (int u = 0; u < U; ++u) {
+    if (num_splits == 0) {
+      if (plan[u].tiles == 0) {
+        plan[u].parts = 0;
+      } else {
+        int c0 = worker_of(plan[u].tile_begin, N, Ca);
+        int c1 = worker_of((long long)plan[u].tile_begin + plan[u].tiles - 1, N, Ca);
+        plan[u].parts = c1 - c0 + 1;
+      }
+    }
+    if (plan[u].parts > 1) {
+      plan[u].slot = slots;
+      slots += plan[u].parts;
+    } else {
+      plan[u].slot = -1;
+    }
+  }
+  return slots;
+}
+
+// Bound on partial slots for a shape: heuristic mode cuts at most C-1 worker boundaries
+// into units, so split units hold at most 2*(C-1) partials; forced mode at most
+// num_splits per unit.
+MLA_HD int max_slots(int units, int num_splits, int C) {
+  if (num_splits > 0) return units * num_splits;
+  int s = 2 * C;
+  return s;
+}
+
+}  // namespace mla

@@ -1,0 +1,235 @@
+// mla_device.cuh -- device-side pieces shared by the decode kernels: launch parameters,
+// the in-kernel evaluation of the split schedule, the status word, and exact decoding of
+// the FP8 / NVFP4 storage codes.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mla_common.cuh"
+
+namespace mla {
+
+struct DecodeParams {
+  const uint16_t* q_nope;     // [B, q_len, H, 512] bf16 bits
+  const uint16_t* q_pe;       // [B, q_len, H, 64]  bf16 bits
+  const uint8_t* cache;       // paged cache (layout per kv_dtype)
+  const int32_t* block_table; // [B, max_pages]
+  const int32_t* seq_lens;    // [B]
+  int max_pages, B, q_len, H, num_pages, page_size;
+  float sm_scale, kv_scale;
+  int kv_dtype, num_splits;
+  int workers;                // scheduling workers C
+  int slots_cap;              // partial slots that fit the workspace
+  uint8_t* ws;                // workspace
+  uint16_t* out;              // [B, q_len, H, 512] bf16 bits
+  float* lse;                 // [B, q_len, H] or nullptr
+};
+
+__device__ __forceinline__ void set_status(uint8_t* ws, unsigned bits) {
+  atomicOr(reinterpret_cast<unsigned*>(ws), bits);
+}
+
+// Bytes per page of the cache.
+__host__ __device__ __forceinline__ size_t page_stride_bytes(int kv_dtype, int page_size) {
+  return kv_dtype == MLA_KV_BF16 ? (size_t)page_size * kDim * 2
+       : kv_dtype == MLA_KV_FP8_E4M3 ? (size_t)page_size * kDim
+       : (size_t)page_size * (kDim / 2 + kDim / kNvfp4Group);
+}
+
+// ---------------------------------------------------------------- exact code decoding
+// E4M3 (OCP FP8 "FN"): sign bit 7, exponent 6..3 (bias 7), mantissa 2..0; exponent 0 is
+// subnormal (m * 2^-9); S.1111.111 is NaN.  Built from the bit fields, exact in fp32.
+__device__ __forceinline__ float e4m3_to_float(unsigned code) {
+  unsigned s = (code & 0x80u) << 24, e = (code >> 3) & 0xFu, m = code & 0x7u;
+  float v;
+  if (e == 0) {
+    v = (float)m * 0.001953125f;  // m * 2^-9
+  } else if (e == 0xF && m == 0x7) {
+    v = __int_as_float(0x7fc00000);
+  } else {
+    v = __int_as_float((int)(((e + 120u) << 23) | (m << 20)));
+  }
+  return __int_as_float(__float_as_int(v) | (int)s);
+}
+// E2M1 (OCP MX FP4): sign bit 3, exponent 2..1 (bias 1), mantissa bit 0; exponent 0 is
+// subnormal (m * 0.5).
+__device__ __forceinline__ float e2m1_to_float(unsigned nib) {
+  unsigned s = (nib & 0x8u) << 28, e = (nib >> 1) & 0x3u, m = nib & 0x1u;
+  float v = e == 0 ? 0.5f * (float)m : __int_as_float((int)(((e + 126u) << 23) | (m << 22)));
+  return __int_as_float(__float_as_int(v) | (int)s);
+}
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __int_as_float(((int)b) << 16);
+}
+__device__ __forceinline__ uint16_t float_to_bf16_bits_rn(float f) {
+  unsigned short r;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(f));
+  return r;
+}
+
+// ---------------------------------------------------------------- schedule on the device
+struct PlanSmem {
+  int N;                     // total tiles (heuristic) or items (forced)
+  int begin[kMaxUnits + 1];  // exclusive prefix of tiles / items
+  int vis[kMaxUnits];        // visible positions per unit
+  int slot[kMaxUnits];       // first partial slot or -1
+};
+
+// Block-wide exclusive scan of vals[0..n) in place; returns the total.  All threads call.
+__device__ inline int block_exclusive_scan(int* vals, int n, int* scratch /*[33]*/) {
+  const int T = blockDim.x * blockDim.y * blockDim.z;
+  const int tid = threadIdx.x + blockDim.x * (threadIdx.y + blockDim.y * threadIdx.z);
+  const int per = (n + T - 1) / T;
+  const int lo = min(n, tid * per), hi = min(n, lo + per);
+  int local = 0;
+  for (int k = lo; k < hi; ++k) local += vals[k];
+  const int lane = tid & 31, warp = tid >> 5, nwarps = (T + 31) >> 5;
+  int incl = local;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += y;
+  }
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nwarps ? scratch[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, wi, d);
+      if (lane >= d) wi += y;
+    }
+    if (lane < nwarps) scratch[lane] = wi - w;  // exclusive warp offsets
+    if (lane == 31) scratch[32] = wi;           // total
+  }
+  __syncthreads();
+  int run = scratch[warp] + incl - local;
+  for (int k = lo; k < hi; ++k) {
+    int v = vals[k];
+    vals[k] = run;
+    run += v;
+  }
+  int total = scratch[32];
+  __syncthreads();
+  return total;
+}
+
+// Evaluates the schedule in shared memory (all threads call).  Sets status bits for
+// malformed seq_lens.  When `write_plan` is set, also stores {parts, slot} per unit into
+// the workspace plan for the split-K reduce.
+__device__ inline void compute_plan(const DecodeParams& p, PlanSmem& pl, int* scratch,
+                                    bool write_plan) {
+  const int T = blockDim.x * blockDim.y * blockDim.z;
+  const int tid = threadIdx.x + blockDim.x * (threadIdx.y + blockDim.y * threadIdx.z);
+  const int U = p.B * p.q_len;
+  unsigned bad = 0;
+  for (int u = tid; u < U; u += T) {
+    int b = u / p.q_len, i = u % p.q_len;
+    int raw = __ldg(p.seq_lens + b);
+    if (raw < 0) bad |= MLA_STATUS_NEG_SEQ_LEN;
+    if ((long long)raw > (long long)p.max_pages * p.page_size) bad |= MLA_STATUS_SEQ_TOO_LONG;
+    int L = clamp_seq_len(raw, p.max_pages, p.page_size);
+    if (L < p.q_len && i == 0) bad |= MLA_STATUS_SEQ_LT_QLEN;
+    int vis = unit_visible(L, p.q_len, i);
+    pl.vis[u] = vis;
+    int tiles = cdiv_i(vis, kTile);
+    pl.begin[u] = p.num_splits > 0 ? (tiles ? cdiv_i(tiles, forced_span_tiles(vis, p.num_splits)) : 0)
+                                   : tiles;
+  }
+  if (bad && write_plan) set_status(p.ws, bad);
+  __syncthreads();
+  int N = block_exclusive_scan(pl.begin, U, scratch);
+  if (tid == 0) {
+    pl.begin[U] = N;
+    pl.N = N;
+  }
+  __syncthreads();
+  // parts per unit -> slot scan (reuse pl.slot as the per-unit split-part count)
+  const int Ca = active_workers(N, p.workers);
+  for (int u = tid; u < U; u += T) {
+    int parts;
+    if (p.num_splits > 0) {
+      parts = pl.begin[u + 1] - pl.begin[u];
+    } else {
+      int tiles = pl.begin[u + 1] - pl.begin[u];
+      parts = tiles ? worker_of(pl.begin[u + 1] - 1, N, Ca) - worker_of(pl.begin[u], N, Ca) + 1
+                    : 0;
+    }
+    pl.slot[u] = parts > 1 ? parts : 0;
+    if (write_plan) {
+      int2* plan = reinterpret_cast<int2*>(p.ws + kPlanOffset);
+      plan[u].x = parts;  // slot written below
+    }
+  }
+  __syncthreads();
+  block_exclusive_scan(pl.slot, U, scratch);
+  for (int u = tid; u < U; u += T) {
+    int parts = p.num_splits > 0 ? pl.begin[u + 1] - pl.begin[u]
+              : (pl.begin[u + 1] > pl.begin[u]
+                     ? worker_of(pl.begin[u + 1] - 1, N, Ca) - worker_of(pl.begin[u], N, Ca) + 1
+                     : 0);
+    if (parts <= 1) pl.slot[u] = -1;
+    if (write_plan) {
+      int2* plan = reinterpret_cast<int2*>(p.ws + kPlanOffset);
+      plan[u].y = pl.slot[u];
+    }
+  }
+  __syncthreads();
+}
+
+// One work item: unit u, token range [tok_lo, tok_hi) of its visible KV, partial slot
+// (or -1 = final output written directly).
+struct WorkItem {
+  int u, tok_lo, tok_hi, slot;
+};
+
+// Smallest index k in [0, n] with a[k] > x, for a non-decreasing a.
+__device__ __forceinline__ int upper_bound_i(const int* a, int n, int x) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    int mid = (lo + hi) >> 1;
+    if (a[mid] <= x) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+// Iterates worker c's items in order, calling f(WorkItem).
+template <class F>
+__device__ inline void for_each_item(const DecodeParams& p, const PlanSmem& pl, int c, F&& f) {
+  const int U = p.B * p.q_len;
+  const int C = p.workers;
+  const int N = pl.N;
+  if (N <= 0) return;
+  if (p.num_splits > 0) {
+    for (int j = c; j < N; j += C) {
+      int u = upper_bound_i(pl.begin, U + 1, j) - 1;
+      int k = j - pl.begin[u];
+      int vis = pl.vis[u];
+      int span = forced_span_tiles(vis, p.num_splits);
+      int tiles = cdiv_i(vis, kTile);
+      int lo = k * span, hi = min((k + 1) * span, tiles);
+      WorkItem it{u, lo * kTile, min(hi * kTile, vis), pl.slot[u] >= 0 ? pl.slot[u] + k : -1};
+      f(it);
+    }
+  } else {
+    const int Ca = active_workers(N, C);
+    if (c >= Ca) return;
+    long long s = worker_begin(c, N, Ca), e = worker_begin(c + 1, N, Ca);
+    if (s >= e) return;
+    int u = upper_bound_i(pl.begin, U + 1, (int)s) - 1;
+    long long t = s;
+    while (t < e) {
+      while (pl.begin[u + 1] <= t) ++u;
+      int tb = pl.begin[u], te = pl.begin[u + 1];
+      int lo = (int)(t - tb), hi = (int)(min(e, (long long)te) - tb);
+      int slot = pl.slot[u] >= 0 ? pl.slot[u] + (c - worker_of(tb, N, Ca)) : -1;
+      WorkItem it{u, lo * kTile, min(hi * kTile, pl.vis[u]), slot};
+      f(it);
+      t = min(e, (long long)te);
+    }
+  }
+}
+
+}  // namespace mla

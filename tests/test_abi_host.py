@@ -1,0 +1,140 @@
+"""CPU-side checks of the C ABI: the library loads and exports every declared symbol, host
+validation rejects bad arguments before touching the GPU, and the split schedule the
+kernels evaluate (mirrored on the host) covers every KV tile exactly once."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from mla_latent_kv_split_gb300 import binding as mb
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(mb.LIB_PATH):
+        from mla_latent_kv_split_gb300 import build
+        build.build()
+    return mb.lib()
+
+
+def _declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", fn)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(mla_[a-z0-9_]+)\s*\(", txt, flags=re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol(L):
+    declared = _declared_functions()
+    assert len(declared) >= 8, declared
+    for name in declared:
+        assert hasattr(L, name), name
+    assert set(mb.EXPORTED) <= set(declared)
+    assert L.mla_decode_abi_version() == 1
+    for code in range(6):
+        assert L.mla_status_string(code).decode().startswith("MLA_")
+
+
+def _call(L, **over):
+    a = dict(q_nope=16, q_pe=16, kv=128, bt=16, max_pages=4, sl=16, B=1, q_len=1, H=16, num_pages=4,
+             page_size=64, sm_scale=0.1, kv_dtype=0, kv_scale=1.0, num_splits=0, ws=256, ws_bytes=1 << 30,
+             out=16, lse=16, stream=None)
+    a.update(over)
+    return L.mla_decode(a["q_nope"], a["q_pe"], a["kv"], a["bt"], a["max_pages"], a["sl"], a["B"], a["q_len"],
+                        a["H"], a["num_pages"], a["page_size"], a["sm_scale"], a["kv_dtype"], a["kv_scale"],
+                        a["num_splits"], a["ws"], a["ws_bytes"], a["out"], a["lse"], a["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(H=24), 2), (dict(H=0), 1), (dict(H=256), 2), (dict(page_size=16), 2), (dict(page_size=128), 2),
+    (dict(q_len=0), 1), (dict(q_len=9), 2), (dict(B=-1), 1), (dict(B=1025), 2), (dict(kv_dtype=7), 1),
+    (dict(sm_scale=float("nan")), 1), (dict(kv_dtype=1, kv_scale=0.0), 1), (dict(kv_dtype=1, kv_scale=float("inf")), 1),
+    (dict(num_splits=-1), 1), (dict(max_pages=0), 1), (dict(num_pages=0), 1),
+    (dict(q_nope=None), 1), (dict(kv=None), 1), (dict(ws=None), 1), (dict(out=None), 1),
+    (dict(q_nope=18), 1), (dict(kv=144), 1), (dict(ws=128), 1), (dict(max_pages=1 << 30), 2),
+])
+def test_host_validation_rejects_before_launch(L, over, code):
+    assert _call(L, **over) == code
+
+
+def test_empty_batch_is_a_noop(L):
+    assert _call(L, B=0, q_nope=None, q_pe=None, kv=None, bt=None, sl=None, ws=None, out=None, lse=None) == 0
+
+
+def _check_plan(seq_lens, q_len, ps, num_splits, C, max_pages=None):
+    seq_lens = np.asarray(seq_lens, dtype=np.int32)
+    if max_pages is None:
+        max_pages = max(1, int(-(-max(int(seq_lens.max()), 1) // ps)))
+    pl = mb.mla_decode_plan_host(seq_lens, q_len, max_pages, ps, num_splits, C)
+    U = len(seq_lens) * q_len
+    vis = np.array([oracle.visible_len(min(max(int(seq_lens[u // q_len]), 0), max_pages * ps), q_len, u % q_len)
+                    for u in range(U)])
+    tiles = -(-vis // 64)
+    assert np.array_equal(pl["tiles"], tiles)
+    # slots: contiguous, disjoint, only for split units
+    used = 0
+    for u in range(U):
+        if pl["parts"][u] > 1:
+            assert pl["slot"][u] == used
+            used += pl["parts"][u]
+        else:
+            assert pl["slot"][u] == -1
+        assert pl["parts"][u] == 0 if tiles[u] == 0 else pl["parts"][u] >= 1
+    assert used == pl["slots_used"]
+    if num_splits > 0:
+        for u in range(U):
+            if tiles[u]:
+                assert pl["parts"][u] == len(oracle.forced_split_ranges(int(vis[u]), num_splits))
+    else:
+        assert used <= 2 * C
+        # brute force: assign tiles to workers by the balanced rule and count parts
+        N = int(tiles.sum())
+        Ca = min(C, N)
+        owner = np.empty(N, dtype=np.int64)
+        for c in range(Ca):
+            owner[c * N // Ca:(c + 1) * N // Ca] = c
+        t0 = 0
+        for u in range(U):
+            if tiles[u]:
+                assert pl["parts"][u] == len(set(owner[t0:t0 + tiles[u]].tolist()))
+            t0 += tiles[u]
+        # balance: every active worker gets floor or ceil of N / Ca tiles
+        if N:
+            counts = np.bincount(owner, minlength=Ca)
+            assert counts.max() - counts.min() <= 1
+    return pl
+
+
+@pytest.mark.parametrize("C", [1, 2, 5, 76, 300])
+def test_plan_heuristic_covers_and_balances(L, C):
+    rng = np.random.default_rng(C)
+    for trial in range(5):
+        B = int(rng.integers(1, 40))
+        q_len = int(rng.integers(1, 5))
+        seq = rng.integers(0, 5000, size=B)
+        _check_plan(seq, q_len, 64, 0, C)
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 7])
+def test_plan_forced_splits(L, n):
+    _check_plan([256, 1, 0, 700, 64, 65], 1, 64, n, 76)
+    _check_plan([256, 9, 300], 4, 32, n, 3)
+
+
+def test_plan_tiny_contiguous_two_splits(L):
+    pl = _check_plan([256], 1, 64, 2, 76)
+    assert pl["parts"][0] == 2 and pl["slots_used"] == 2
+
+
+def test_plan_clamps_and_negative_lengths(L):
+    pl = _check_plan([-5, 10 ** 6, 3], 2, 64, 0, 4, max_pages=2)
+    assert pl["tiles"][0] == 0 and pl["tiles"][1] == 0  # seq_len -5 -> nothing visible
+    assert pl["tiles"][2] == 2 and pl["tiles"][3] == 2  # clamped to 128: 127 and 128 visible
