@@ -164,6 +164,35 @@ mla_status_t mla_decode_plan_host(const int32_t *seq_lens, int B, int q_len, int
                                   int32_t *unit_tile_begin, int32_t *unit_tiles,
                                   int32_t *unit_parts, int32_t *unit_slot, int32_t *slots_used);
 
+/*
+ * mla_decode_no_alloc -- mla_decode for callers that cannot allocate device memory.
+ * The source pages have no counterpart to this entry point; it exists for users of this
+ * library whose code may not call cudaMalloc: for example a plugin or callback that runs
+ * inside another runtime which owns every device allocation, or a process that must
+ * keep its device footprint fixed after start-up and so cannot create a workspace.
+ *
+ * Same arguments and results as mla_decode, minus the workspace: the scratch is a
+ * file-scope static device buffer of MLA_NO_ALLOC_SCRATCH_BYTES inside this library.
+ * Every GPU on which the library's no-alloc code is loaded holds that buffer until the
+ * process exits.  No call allocates or frees memory.
+ *   - The first call on each device looks up the buffer's device address with that
+ *     device current; make that first call before any stream capture.
+ *   - A shape whose workspace (mla_decode_workspace_size) exceeds
+ *     MLA_NO_ALLOC_SCRATCH_BYTES returns MLA_ERR_WORKSPACE_TOO_SMALL; nothing is enqueued.
+ *   - All calls on a device share the one buffer, which keeps the last call's contents;
+ *     each call resets the status word it needs zeroed and overwrites the rest.  Calls
+ *     that overlap on the GPU (other streams, other host threads) race on the buffer:
+ *     the caller must order them.
+ *   - *scratch_used (may be NULL) receives the buffer's device address, e.g. for
+ *     mla_decode_read_status after the call.
+ */
+#define MLA_NO_ALLOC_SCRATCH_BYTES (48u << 20) /* 48 MiB per device */
+mla_status_t mla_decode_no_alloc(const void *q_nope, const void *q_pe, const void *kv_cache,
+                                 const int32_t *block_table, int max_pages, const int32_t *seq_lens,
+                                 int B, int q_len, int H, int num_pages, int page_size,
+                                 float sm_scale, int kv_dtype, float kv_scale, int num_splits,
+                                 void *out, float *lse, mla_stream_t stream, void **scratch_used);
+
 #ifdef __cplusplus
 }
 #endif

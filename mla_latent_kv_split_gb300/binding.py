@@ -25,6 +25,7 @@ STATUS_BITS = {
 EXPORTED = (
     "mla_decode_abi_version", "mla_status_string", "mla_decode_workspace_size", "mla_decode",
     "mla_splitk_reduce", "mla_decode_read_status", "mla_decode_num_workers", "mla_decode_plan_host",
+    "mla_decode_no_alloc",
 )
 
 
@@ -64,6 +65,9 @@ def lib() -> ctypes.CDLL:
             i32p = ctypes.POINTER(ctypes.c_int32)
             h.mla_decode_plan_host.restype = I
             h.mla_decode_plan_host.argtypes = [i32p, I, I, I, I, I, I, i32p, i32p, i32p, i32p, i32p]
+            h.mla_decode_no_alloc.restype = I
+            h.mla_decode_no_alloc.argtypes = [P, P, P, P, I, P, I, I, I, I, I, F, I, F, I, P, P, P,
+                                              ctypes.POINTER(P)]
             _handle = h
         return _handle
 
@@ -167,3 +171,28 @@ def mla_decode_plan_host(seq_lens, q_len: int, max_pages: int, page_size: int, n
         sl.ctypes.data_as(i32p), B, q_len, max_pages, page_size, num_splits, workers,
         *[a.ctypes.data_as(i32p) for a in arrs], ctypes.byref(used)))
     return dict(tile_begin=arrs[0], tiles=arrs[1], parts=arrs[2], slot=arrs[3], slots_used=used.value)
+
+
+def mla_decode_no_alloc(q_nope, q_pe, kv_cache, block_table, seq_lens, sm_scale: float, kv_dtype="bf16",
+                        kv_scale: float = 1.0, num_splits: int = 0, page_size: int | None = None,
+                        num_pages: int | None = None, out=None, lse=None, stream=None):
+    """Calls ``mla_decode_no_alloc`` (scratch in the library's static device buffer; for
+    callers that cannot allocate).  Returns ``(out, lse, scratch_address)``; ``out``/``lse``
+    are allocated with torch here only when not given."""
+    import torch
+    B, q_len, H, _ = q_nope.shape
+    kd = KV_DTYPE[kv_dtype] if isinstance(kv_dtype, str) else int(kv_dtype)
+    if page_size is None:
+        page_size = kv_cache.shape[1]
+    if num_pages is None:
+        num_pages = kv_cache.shape[0]
+    if out is None:
+        out = torch.empty((B, q_len, H, 512), dtype=torch.bfloat16, device=q_nope.device)
+    if lse is None:
+        lse = torch.empty((B, q_len, H), dtype=torch.float32, device=q_nope.device)
+    scratch = ctypes.c_void_p(0)
+    _check("mla_decode_no_alloc", lib().mla_decode_no_alloc(
+        _ptr(q_nope), _ptr(q_pe), _ptr(kv_cache), _ptr(block_table), int(block_table.shape[1]),
+        _ptr(seq_lens), B, q_len, H, int(num_pages), int(page_size), float(sm_scale), kd,
+        float(kv_scale), int(num_splits), _ptr(out), _ptr(lse), _stream_ptr(stream), ctypes.byref(scratch)))
+    return out, lse, scratch.value
