@@ -16,6 +16,8 @@
 
 namespace mla {
 cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t stream);
+int tc_max_clusters();
 cudaError_t launch_splitk_reduce(const uint8_t* ws, int U, int H, int slots_cap, uint16_t* out,
                                  float* lse, cudaStream_t stream, bool pdl);
 }  // namespace mla
@@ -26,7 +28,8 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int g_workers[kMaxDevices] = {0};
 
-// Scheduling workers on the current device: one per pair of SMs.
+// Scheduling workers on the current device: one per co-resident 2-CTA cluster of the
+// tensor-core kernel (at most one per pair of SMs).
 cudaError_t current_workers(int* workers) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -37,7 +40,10 @@ cudaError_t current_workers(int* workers) {
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    g_workers[dev] = sms >= 2 ? sms / 2 : 1;
+    int w = sms >= 2 ? sms / 2 : 1;
+    int clusters = mla::tc_max_clusters();
+    if (clusters > 0 && clusters < w) w = clusters;
+    g_workers[dev] = w;
   }
   *workers = g_workers[dev];
   return cudaSuccess;
@@ -179,7 +185,8 @@ MLA_EXPORT mla_status_t mla_decode(const void* q_nope, const void* q_pe, const v
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(workspace, 0, 16, s) != cudaSuccess) return MLA_ERR_CUDA;
-  if (mla::launch_decode_simt(p, s) != cudaSuccess) return MLA_ERR_CUDA;
+  cudaError_t le = kv_dtype == MLA_KV_BF16 ? mla::launch_decode_tc(p, s) : mla::launch_decode_simt(p, s);
+  if (le != cudaSuccess) return MLA_ERR_CUDA;
   if (mla::launch_splitk_reduce(p.ws, U, H, p.slots_cap, p.out, lse, s, true) != cudaSuccess)
     return MLA_ERR_CUDA;
   return MLA_OK;
