@@ -74,6 +74,7 @@ struct PlanSmem {
   int begin[kMaxUnits + 1];  // exclusive prefix of tiles / items
   int vis[kMaxUnits];        // visible positions per unit
   int slot[kMaxUnits];       // first partial slot or -1
+  int pref[kMaxUnits];       // exclusive prefix of the partial slots of split units
 };
 
 // Block-wide exclusive scan of vals[0..n) in place; returns the total.  All threads call.
@@ -165,6 +166,7 @@ __device__ inline void compute_plan(const DecodeParams& p, PlanSmem& pl, int* sc
   }
   __syncthreads();
   block_exclusive_scan(pl.slot, U, scratch);
+  for (int u = tid; u < U; u += T) pl.pref[u] = pl.slot[u];
   for (int u = tid; u < U; u += T) {
     int parts = p.num_splits > 0 ? pl.begin[u + 1] - pl.begin[u]
               : (pl.begin[u + 1] > pl.begin[u]
@@ -228,6 +230,91 @@ __device__ inline void for_each_item(const DecodeParams& p, const PlanSmem& pl, 
       WorkItem it{u, lo * kTile, min(hi * kTile, pl.vis[u]), slot};
       f(it);
       t = min(e, (long long)te);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- cursor form
+// Where worker c starts in the schedule: its first unit, that unit's first tile (heuristic
+// mode) or first item (forced mode), the partial slots used by earlier units, and the
+// total tile / item count.  From these the worker walks its items reading only seq_lens,
+// so the per-unit arrays of PlanSmem need not stay resident.
+struct WorkerStart {
+  int u0, base0, slot0, N;
+};
+
+__device__ inline WorkerStart worker_start(const DecodeParams& p, const PlanSmem& pl, int c) {
+  const int U = p.B * p.q_len;
+  WorkerStart w{0, 0, 0, pl.N};
+  if (pl.N <= 0) return w;
+  int first;
+  if (p.num_splits > 0) {
+    first = c;
+  } else {
+    const int Ca = active_workers(pl.N, p.workers);
+    if (c >= Ca) return w;
+    first = (int)worker_begin(c, pl.N, Ca);
+  }
+  if (first >= pl.N) return w;
+  const int u = upper_bound_i(pl.begin, U + 1, first) - 1;
+  w.u0 = u;
+  w.base0 = pl.begin[u];
+  w.slot0 = pl.pref[u];
+  return w;
+}
+
+__device__ __forceinline__ int unit_visible_dev(const DecodeParams& p, int u) {
+  const int b = u / p.q_len, i = u % p.q_len;
+  return unit_visible(clamp_seq_len(__ldg(p.seq_lens + b), p.max_pages, p.page_size), p.q_len, i);
+}
+
+// Same items, same order as for_each_item, walking units from the worker's start.
+template <class F>
+__device__ inline void for_each_item_cursor(const DecodeParams& p, const WorkerStart& w, int c, F&& f) {
+  const int N = w.N;
+  if (N <= 0) return;
+  if (p.num_splits > 0) {
+    const int C = p.workers;
+    int u = w.u0, ib = w.base0, sacc = w.slot0;
+    for (int j = c; j < N; j += C) {
+      int vis, tiles, parts, span;
+      for (;;) {
+        vis = unit_visible_dev(p, u);
+        tiles = cdiv_i(vis, kTile);
+        span = forced_span_tiles(vis, p.num_splits);
+        parts = tiles ? cdiv_i(tiles, span) : 0;
+        if (ib + parts > j) break;
+        sacc += parts > 1 ? parts : 0;
+        ib += parts;
+        ++u;
+      }
+      const int k = j - ib;
+      const int lo = k * span, hi = min((k + 1) * span, tiles);
+      f(WorkItem{u, lo * kTile, min(hi * kTile, vis), parts > 1 ? sacc + k : -1});
+    }
+  } else {
+    const int Ca = active_workers(N, p.workers);
+    if (c >= Ca) return;
+    const long long s = worker_begin(c, N, Ca), e = worker_begin(c + 1, N, Ca);
+    if (s >= e) return;
+    int u = w.u0, sacc = w.slot0;
+    long long tb = w.base0, t = s;
+    while (t < e) {
+      const int vis = unit_visible_dev(p, u);
+      const int tiles = cdiv_i(vis, kTile);
+      const long long te = tb + tiles;
+      const int parts = tiles ? worker_of(te - 1, N, Ca) - worker_of(tb, N, Ca) + 1 : 0;
+      if (te > t) {
+        const int lo = (int)(t - tb), hi = (int)(min(e, te) - tb);
+        const int slot = parts > 1 ? sacc + (c - worker_of(tb, N, Ca)) : -1;
+        f(WorkItem{u, lo * kTile, min(hi * kTile, vis), slot});
+        t = min(e, te);
+      }
+      if (t >= te) {
+        sacc += parts > 1 ? parts : 0;
+        tb = te;
+        ++u;
+      }
     }
   }
 }
