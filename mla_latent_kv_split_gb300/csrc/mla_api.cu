@@ -15,7 +15,6 @@
 #define MLA_EXPORT extern "C" __attribute__((visibility("default")))
 
 namespace mla {
-cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t stream);
 int tc_max_clusters();
 cudaError_t launch_splitk_reduce(const uint8_t* ws, int U, int H, int slots_cap, uint16_t* out,
@@ -185,7 +184,7 @@ MLA_EXPORT mla_status_t mla_decode(const void* q_nope, const void* q_pe, const v
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(workspace, 0, 16, s) != cudaSuccess) return MLA_ERR_CUDA;
-  cudaError_t le = kv_dtype == MLA_KV_BF16 ? mla::launch_decode_tc(p, s) : mla::launch_decode_simt(p, s);
+  cudaError_t le = mla::launch_decode_tc(p, s);
   if (le != cudaSuccess) return MLA_ERR_CUDA;
   if (mla::launch_splitk_reduce(p.ws, U, H, p.slots_cap, p.out, lse, s, true) != cudaSuccess)
     return MLA_ERR_CUDA;

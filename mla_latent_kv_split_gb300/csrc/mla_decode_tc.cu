@@ -15,12 +15,15 @@
 //   producer warp   TMA-gathers the tile's pages (block table -> page rows) into a
 //                   4-stage ring: 4 boxes of 64 tokens x 64 latent columns (128-byte
 //                   swizzle) + 1 box of 64 tokens x 32 rope columns (64-byte swizzle)
-//   fix-up warp     hands every landed tile to the MMA warp, first zeroing cache rows that
-//                   are masked (ragged tail, invalid page) so that garbage (even NaN)
-//                   there cannot reach P.V
+//                   (FP8: the E4M3 bytes of those columns; NVFP4: whole pages, packed
+//                   E2M1 data plus E4M3 scales, into the tail of the stage)
 //   MMA warp        S[128 x 64] = Q[128 x 288] (in TMEM) . K^T       (18 MMAs, K = 16)
 //                   O[128 x 256] += P[128 x 64] (in TMEM) . V[64 x 256] (4 MMAs, N = 256)
-//   sender warps    one warpgroup; thread = head row: loads the row's 64 partial scores
+//   sender warps    one warpgroup.  (1) Prepares each landed tile for the MMAs: zeroes the
+//                   rows that are masked (ragged tail, invalid page) so that garbage, even
+//                   NaN, cannot reach P.V, and for FP8 / NVFP4 decodes the raw bytes in place
+//                   into f16 (exact for both formats) in the same swizzled layout.
+//                   (2) Thread = head row: loads the row's 64 partial scores
 //                   from TMEM and pushes them into the peer CTA's exchange buffer with
 //                   asynchronous stores that complete on the peer's mbarrier (the link is
 //                   the slowest path of the exchange, so it gets warps of its own)
@@ -40,6 +43,7 @@
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "mla_device.cuh"
 #include "mla_ptx.cuh"
@@ -60,25 +64,30 @@ constexpr int kXBytes = 128 * kXWordsPerRow * 4;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0, kTmemS = 256, kTmemQ = 384;  // S buffers at kTmemS + 64 * (g & 1)
 constexpr int kQRopeBytes = 128 * 64;  // Q rope: 128 rows x 32 bf16, K-major, 64-byte swizzle
-constexpr int kPBytes = 128 * 128;     // P: 128 rows x 64 tokens bf16, K-major, 128-byte swizzle
+constexpr int kPBytes = 128 * 128;     // P: 128 rows x 64 tokens 16-bit, K-major, 128-byte swizzle
+// Raw bytes of quantized tiles sit in the tail of a stage and are decoded in place:
+constexpr int kRawFp8 = kStageBytes - kTileN * 288;    // FP8: 256 latent + 32 rope bytes per row
+constexpr int kRawFp8Rope = kRawFp8 + kTileN * 256;
+constexpr int kRawFp4 = kStageBytes - kTileN * 324;    // NVFP4: whole pages (288 data + 36 scale B per token)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;       // log2 units: P stays below 2^8
 
 // warp roles
-constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpFixup = 2, kWarpRelay = 3, kWarpSender0 = 4, kWarpSoftmax0 = 8;
+constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpRelay = 3, kWarpSender0 = 4, kWarpSoftmax0 = 8;
 constexpr int kSenderThreads = 128;   // warps 4..7
 constexpr int kSoftmaxThreads = 256;  // warps 8..15
 // Registers per thread: the launch gives every thread kLaunchRegs; the control warpgroup
 // (warps 0..3) drops to kCtrlRegs, the sender warpgroup to kSenderRegs, and the two softmax
 // warpgroups rise to kSoftmaxRegs.  The sum must not exceed 512 * kLaunchRegs (65,536).
-constexpr uint32_t kLaunchRegs = 128, kCtrlRegs = 64, kSenderRegs = 96, kSoftmaxRegs = 176;
+constexpr uint32_t kLaunchRegs = 128, kCtrlRegs = 64, kSenderRegs = 128, kSoftmaxRegs = 160;
 static_assert(128 * kCtrlRegs + 128 * kSenderRegs + 256 * kSoftmaxRegs <= 512 * kLaunchRegs,
               "register split exceeds the launch budget");
 
 struct Bars {
   uint64_t kv_full[kStages];   // TMA bytes landed
-  uint64_t kv_ready[kStages];  // fix-up warp passed the tile (masked rows zeroed)
+  uint64_t kv_ready[kStages];  // senders prepared the tile (masked rows zeroed, quantized data decoded)
+  uint64_t deq;                // senders read every raw byte of a tile (before decoding in place)
   uint64_t kv_empty[kStages];  // P.V of the tile completed: stage reusable
   uint64_t s_full[2];          // S MMAs of a buffer completed
   uint64_t s_free[2];          // senders and softmax read a buffer's S
@@ -150,6 +159,14 @@ __device__ __forceinline__ TileInfo tile_info(const DecodeParams& p, int b, int 
 }
 __device__ __forceinline__ bool tile_needs_fixup(const TileInfo& ti) { return ti.rowmask != ~0ull; }
 
+// Two bf16 values -> two f16 (exact for |x| in [2^-14, 65504]; smaller magnitudes round to
+// f16 subnormals, larger ones overflow and are reported).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v, bool& out_of_range) {
+  const float lo = __uint_as_float(v << 16), hi = __uint_as_float(v & 0xFFFF0000u);
+  out_of_range |= fabsf(lo) > 65504.f || fabsf(hi) > 65504.f;
+  return ptx::pack_f16x2(lo, hi);
+}
+
 // fp32 bit pattern rounded to its top 24 bits (sign, exponent, 15 mantissa bits), nearest.
 __device__ __forceinline__ uint32_t round24(uint32_t bits) { return (bits + 0x80u) & 0xFFFFFF00u; }
 // Four fp32 values -> three words holding their rounded top 24 bits.
@@ -199,6 +216,9 @@ __device__ __forceinline__ uint32_t tile_half_mask(const DecodeParams& p, const 
   return (uint32_t)(m >> (32 * h));
 }
 
+// KV: cache format (MLA_KV_BF16 / MLA_KV_FP8_E4M3 / MLA_KV_NVFP4).  The MMAs run in bf16 for a
+// bf16 cache and in f16 for the quantized ones (E4M3 and E2M1 x E4M3 are exact in f16).
+template <int KV>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope,
                      const DecodeParams p) {
@@ -231,11 +251,12 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
   const uint32_t b_mma_final = ptx::smem_u32(&S.bars.mma_final);
   const uint32_t b_mx = ptx::smem_u32(&S.bars.mx[0]), b_lsum = ptx::smem_u32(&S.bars.lsum);
   const uint32_t b_x_read = ptx::smem_u32(&S.bars.x_read[0]);
+  const uint32_t b_deq = ptx::smem_u32(&S.bars.deq);
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(b_kv_full + 8 * s, 1);
-      ptx::mbar_init(b_kv_ready + 8 * s, 1);
+      ptx::mbar_init(b_kv_ready + 8 * s, kSenderThreads);
       ptx::mbar_init(b_kv_empty + 8 * s, 1);
     }
     for (int s = 0; s < 2; ++s) {
@@ -253,6 +274,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       ptx::mbar_init(b_x_read + 8 * s, kSoftmaxThreads / 32);
     }
     ptx::mbar_init(b_lsum, kSoftmaxThreads);
+    ptx::mbar_init(b_deq, kSenderThreads);
     ptx::mbar_init(b_mma_final, 1);
     S.abort_flag = 0;
     ptx::fence_mbar_init_cluster();
@@ -261,7 +283,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
     ptx::tmem_alloc(ptx::smem_u32(&S.tmem_base), kTmemCols);
     ptx::tmem_relinquish();
   }
-  if (warp == kWarpProducer && lane == 0) {
+  if (KV != MLA_KV_NVFP4 && warp == kWarpProducer && lane == 0) {
     ptx::prefetch_tmap(&tm_lat);
     ptx::prefetch_tmap(&tm_rope);
   }
@@ -285,9 +307,12 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
           const int st = g % kStages;
           if (g >= kStages && !ptx::mbar_wait(b_kv_empty + 8 * st, ((g / kStages) - 1) & 1, abort_flag)) return;
           const TileInfo ti = tile_info(p, b, t0, it.tok_hi);
+          const uint32_t page_bytes = KV == MLA_KV_BF16 ? (uint32_t)p.page_size * (4 * 128 + 64)
+                                    : KV == MLA_KV_FP8_E4M3 ? (uint32_t)p.page_size * 288
+                                                            : (uint32_t)p.page_size * 324;
           uint32_t bytes = 0;
           for (int j = 0; j < ti.npages; ++j) {
-            if (ti.page_ok[j]) bytes += (uint32_t)p.page_size * (4 * 128 + 64);
+            if (ti.page_ok[j]) bytes += page_bytes;
             else set_status(p.ws, MLA_STATUS_PAGE_OUT_OF_RANGE);
           }
           ptx::mbar_arrive_expect_tx(b_kv_full + 8 * st, bytes);
@@ -296,11 +321,19 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
             if (!ti.page_ok[j]) continue;
             const int y = ti.page[j] * p.page_size;
             const int roff = j * p.page_size;
+            if (KV == MLA_KV_BF16) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              ptx::tma_load_2d(dst + k * kLatBox + roff * 128, &tm_lat, 256 * (int)cr + 64 * k, y,
-                               b_kv_full + 8 * st);
-            ptx::tma_load_2d(dst + 4 * kLatBox + roff * 64, &tm_rope, 512 + 32 * (int)cr, y, b_kv_full + 8 * st);
+              for (int k = 0; k < 4; ++k)
+                ptx::tma_load_2d(dst + k * kLatBox + roff * 128, &tm_lat, 256 * (int)cr + 64 * k, y,
+                                 b_kv_full + 8 * st);
+              ptx::tma_load_2d(dst + 4 * kLatBox + roff * 64, &tm_rope, 512 + 32 * (int)cr, y, b_kv_full + 8 * st);
+            } else if (KV == MLA_KV_FP8_E4M3) {
+              ptx::tma_load_2d(dst + kRawFp8 + roff * 256, &tm_lat, 256 * (int)cr, y, b_kv_full + 8 * st);
+              ptx::tma_load_2d(dst + kRawFp8Rope + roff * 32, &tm_rope, 512 + 32 * (int)cr, y, b_kv_full + 8 * st);
+            } else {
+              ptx::bulk_load(dst + kRawFp4 + j * page_bytes, p.cache + (size_t)ti.page[j] * page_bytes, page_bytes,
+                             b_kv_full + 8 * st);
+            }
           }
         }
       });
@@ -310,32 +343,6 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
         ptx::mbar_wait(b_kv_full + 8 * (gg % kStages), (gg / kStages) & 1, abort_flag, false, 100000000ull);
       }
     }
-  } else if (warp == kWarpFixup) {
-    // ------------------------------------------------------------------ masked-row fix-up
-    ptx::regs_dec<kCtrlRegs>();
-    int g = 0;
-    for_each_item_cursor(p, wst, worker, [&](const WorkItem& it) {
-      const int b = it.u / p.q_len;
-      for (int t0 = it.tok_lo; t0 < it.tok_hi; t0 += kTileN, ++g) {
-        if (*abort_flag) return;
-        const TileInfo ti = tile_info(p, b, t0, it.tok_hi);
-        const int st = g % kStages;
-        if (!ptx::mbar_wait(b_kv_full + 8 * st, (g / kStages) & 1, abort_flag)) return;
-        if (tile_needs_fixup(ti)) {
-          uint8_t* base = S.stage[st];
-          for (int idx = lane; idx < kTileN * 36; idx += 32) {
-            const int r = idx / 36, c = idx % 36;
-            if ((ti.rowmask >> r) & 1ull) continue;
-            uint8_t* ptr = c < 32 ? base + (c >> 3) * kLatBox + r * 128 + (c & 7) * 16
-                                  : base + 4 * kLatBox + r * 64 + (c - 32) * 16;
-            *reinterpret_cast<uint4*>(ptr) = make_uint4(0u, 0u, 0u, 0u);
-          }
-          ptx::fence_proxy_async_smem();
-        }
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(b_kv_ready + 8 * st);
-      }
-    });
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------------ MMA issuer
     ptx::regs_dec<kCtrlRegs>();
@@ -343,8 +350,9 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
     // cache tile has landed and the softmax has read the previous scores, independently
     // of the P.V of earlier tiles, which are issued whenever their P is ready.
     if (lane == 0) {
-      constexpr uint32_t idesc_s = ptx::idesc_f16(1, 0, 128, kTileN);  // K-major B (cache rows)
-      constexpr uint32_t idesc_o = ptx::idesc_f16(1, 1, 128, 256);     // MN-major B (V columns)
+      constexpr uint32_t ab = KV == MLA_KV_BF16 ? 1u : 0u;                 // bf16 / f16 operands
+      constexpr uint32_t idesc_s = ptx::idesc_f16(ab, 0, 128, kTileN);  // K-major B (cache rows)
+      constexpr uint32_t idesc_o = ptx::idesc_f16(ab, 1, 128, 256);     // MN-major B (V columns)
       const uint32_t stage0 = ptx::smem_u32(S.stage[0]);
       // base descriptors of stage 0; stage st adds st * kStageBytes to the address field
       const uint64_t kdesc0 = ptx::umma_desc(stage0, 16, 1024, 2);               // K rows, 128 B swizzle
@@ -432,35 +440,118 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
     const uint32_t t_s0 = tmem + ((uint32_t)(32 * q) << 16) + kTmemS;
     const uint32_t x_peer = ptx::mapa(ptx::smem_u32(&S.xbuf[0][0][0]), peer);
     const uint32_t bx_full_peer = ptx::mapa(b_x_full, peer);
+    const int tq = (warp - kWarpSender0) * 32 + lane;  // 0..127
+    const int pr = tq >> 1, phf = tq & 1;              // prepare: row and half-row (18 chunks of 8)
+
+    // (1) Tile k has landed: zero masked rows; decode FP8 / NVFP4 bytes in place to f16.
+    auto prepare = [&](int k, const TileInfo& ti) -> bool {
+      const int st = k % kStages;
+      if (!ptx::mbar_wait(b_kv_full + 8 * st, (k / kStages) & 1, abort_flag)) return false;
+      uint8_t* base = S.stage[st];
+      const bool valid = (ti.rowmask >> pr) & 1ull;
+      // destination of 16-byte chunk c (8 values) of row pr in the swizzled operand layout
+      auto chunk_ptr = [&](int c) -> uint4* {
+        return reinterpret_cast<uint4*>(c < 32 ? base + (c >> 3) * kLatBox + pr * 128 + (((c & 7) ^ (pr & 7)) * 16)
+                                              : base + 4 * kLatBox + pr * 64 + ((((c - 32) ^ ((pr >> 1) & 3))) * 16));
+      };
+      if (KV == MLA_KV_BF16) {
+        if (!valid) {
+#pragma unroll 1
+          for (int c = 18 * phf; c < 18 * phf + 18; ++c) *chunk_ptr(c) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      } else {
+        // every raw byte this thread needs -> registers, then (after all senders did the
+        // same) the decoded values over the same stage
+        uint32_t raw[18][2];
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 18; ++i) {
+            const int c = 18 * phf + i;
+            if (KV == MLA_KV_FP8_E4M3) {
+              const uint2 v = *reinterpret_cast<const uint2*>(c < 32 ? base + kRawFp8 + pr * 256 + 8 * c
+                                                                     : base + kRawFp8Rope + pr * 32 + 8 * (c - 32));
+              raw[i][0] = v.x;
+              raw[i][1] = v.y;
+            } else {
+              const int ps = p.page_size;
+              const int j = pr / ps, rin = pr - j * ps;
+              const uint8_t* page = base + kRawFp4 + j * ps * 324;
+              const int col0 = c < 32 ? 256 * (int)cr + 8 * c : 512 + 32 * (int)cr + 8 * (c - 32);
+              raw[i][0] = *reinterpret_cast<const uint32_t*>(page + rin * 288 + col0 / 2);
+              raw[i][1] = page[ps * 288 + rin * 36 + col0 / 16];
+            }
+          }
+        }
+        ptx::mbar_arrive(b_deq);
+        if (!ptx::mbar_wait(b_deq, k & 1, abort_flag)) return false;
+#pragma unroll
+        for (int i = 0; i < 18; ++i) {
+          uint4 o = make_uint4(0u, 0u, 0u, 0u);
+          if (valid) {
+            if (KV == MLA_KV_FP8_E4M3) {
+              o.x = ptx::e4m3x2_to_f16x2((uint16_t)(raw[i][0] & 0xFFFFu));
+              o.y = ptx::e4m3x2_to_f16x2((uint16_t)(raw[i][0] >> 16));
+              o.z = ptx::e4m3x2_to_f16x2((uint16_t)(raw[i][1] & 0xFFFFu));
+              o.w = ptx::e4m3x2_to_f16x2((uint16_t)(raw[i][1] >> 16));
+            } else {
+              const uint32_t sc = ptx::e4m3x2_to_f16x2((uint16_t)(raw[i][1] | (raw[i][1] << 8)));
+              o.x = ptx::hmul2(ptx::e2m1x2_to_f16x2(raw[i][0] & 0xFFu), sc);
+              o.y = ptx::hmul2(ptx::e2m1x2_to_f16x2((raw[i][0] >> 8) & 0xFFu), sc);
+              o.z = ptx::hmul2(ptx::e2m1x2_to_f16x2((raw[i][0] >> 16) & 0xFFu), sc);
+              o.w = ptx::hmul2(ptx::e2m1x2_to_f16x2(raw[i][0] >> 24), sc);
+            }
+          }
+          *chunk_ptr(18 * phf + i) = o;
+        }
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive(b_kv_ready + 8 * st);
+      return true;
+    };
+
+    // (2) Tile k's partial scores -> the peer CTA.
+    auto send = [&](int k) -> bool {
+      if (!ptx::mbar_wait(b_s_full + 8 * (k & 1), (k >> 1) & 1, abort_flag)) return false;
+      ptx::tc_fence_after();
+      uint32_t r0[32], r1[32];
+      const uint32_t t_s = t_s0 + 64 * (k & 1);
+      ptx::tmem_ld32(t_s, r0);
+      ptx::tmem_ld32(t_s + 32, r1);
+      ptx::tmem_ld_wait();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(b_s_free + 8 * (k & 1));
+      const int slot = k & 1, use = k >> 1;
+      if (use >= 1 && !ptx::mbar_wait(b_x_empty + 8 * slot, (use - 1) & 1, abort_flag, true)) return false;
+      const uint32_t xp = x_peer + (uint32_t)slot * kXBytes + (uint32_t)row * 16;
+      const uint32_t bar = bx_full_peer + 8 * slot;
+      // 16 values -> 12 packed words -> three 16-byte stores, four times
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const uint32_t* src = h < 2 ? r0 + 16 * h : r1 + 16 * (h - 2);
+        uint32_t pw[12];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          pack24x4(src[4 * j], src[4 * j + 1], src[4 * j + 2], src[4 * j + 3], pw[3 * j], pw[3 * j + 1], pw[3 * j + 2]);
+#pragma unroll
+        for (int j = 0; j < 3; ++j)
+          ptx::st_async_v4(xp + (3 * h + j) * 128 * 16, __uint_as_float(pw[4 * j]), __uint_as_float(pw[4 * j + 1]),
+                           __uint_as_float(pw[4 * j + 2]), __uint_as_float(pw[4 * j + 3]), bar);
+      }
+      return true;
+    };
+
+    // Tile k is prepared one step before tile k-1's scores are sent.
     int g = 0;
+    bool dead = false;
     for_each_item_cursor(p, wst, worker, [&](const WorkItem& it) {
+      const int b = it.u / p.q_len;
       for (int t0 = it.tok_lo; t0 < it.tok_hi; t0 += kTileN, ++g) {
-        if (*abort_flag) return;
-        if (!ptx::mbar_wait(b_s_full + 8 * (g & 1), (g >> 1) & 1, abort_flag)) return;
-        ptx::tc_fence_after();
-        uint32_t r0[32], r1[32];
-        const uint32_t t_s = t_s0 + 64 * (g & 1);
-        ptx::tmem_ld32(t_s, r0);
-        ptx::tmem_ld32(t_s + 32, r1);
-        ptx::tmem_ld_wait();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(b_s_free + 8 * (g & 1));
-        const int slot = g & 1, use = g >> 1;
-        if (use >= 1 && !ptx::mbar_wait(b_x_empty + 8 * slot, (use - 1) & 1, abort_flag, true)) return;
-        const uint32_t xp = x_peer + (uint32_t)slot * kXBytes + (uint32_t)row * 16;
-        const uint32_t bar = bx_full_peer + 8 * slot;
-        uint32_t pw[48];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) pack24x4(r0[4 * j], r0[4 * j + 1], r0[4 * j + 2], r0[4 * j + 3], pw[3 * j], pw[3 * j + 1], pw[3 * j + 2]);
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          pack24x4(r1[4 * j], r1[4 * j + 1], r1[4 * j + 2], r1[4 * j + 3], pw[24 + 3 * j], pw[24 + 3 * j + 1], pw[24 + 3 * j + 2]);
-#pragma unroll
-        for (int k = 0; k < 12; ++k)
-          ptx::st_async_v4(xp + k * 128 * 16, __uint_as_float(pw[4 * k]), __uint_as_float(pw[4 * k + 1]),
-                           __uint_as_float(pw[4 * k + 2]), __uint_as_float(pw[4 * k + 3]), bar);
+        if (dead || *abort_flag) return;
+        const TileInfo ti = tile_info(p, b, t0, it.tok_hi);
+        if (!prepare(g, ti) || (g > 0 && !send(g - 1))) { dead = true; return; }
       }
     });
+    if (!dead && g > 0) send(g - 1);
   } else if (warp >= kWarpSoftmax0) {
     // ------------------------------------------------------------------ softmax + epilogue
     ptx::regs_inc<kSoftmaxRegs>();
@@ -480,12 +571,17 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       const bool real = row < p.H;
       const size_t qrow = ((size_t)b * p.q_len + i) * p.H + (real ? row : 0);
       const uint4* qn = reinterpret_cast<const uint4*>(p.q_nope + qrow * kLatent + 256 * cr + 128 * h2);
+      bool q_range = false;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint4 x = real ? __ldg(qn + c * 8 + k) : make_uint4(0u, 0u, 0u, 0u);
           v[4 * k] = x.x; v[4 * k + 1] = x.y; v[4 * k + 2] = x.z; v[4 * k + 3] = x.w;
+        }
+        if (KV != MLA_KV_BF16) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] = bf16x2_to_f16x2(v[k], q_range);
         }
         ptx::tmem_st32(t_q + 64 * h2 + 32 * c, v);
       }
@@ -495,10 +591,17 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       const uint4* qp = reinterpret_cast<const uint4*>(p.q_pe + qrow * kRope + 32 * cr + 16 * h2);
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
-        const uint4 x = real ? __ldg(qp + k) : make_uint4(0u, 0u, 0u, 0u);
+        uint4 x = real ? __ldg(qp + k) : make_uint4(0u, 0u, 0u, 0u);
+        if (KV != MLA_KV_BF16) {
+          x.x = bf16x2_to_f16x2(x.x, q_range);
+          x.y = bf16x2_to_f16x2(x.y, q_range);
+          x.z = bf16x2_to_f16x2(x.z, q_range);
+          x.w = bf16x2_to_f16x2(x.w, q_range);
+        }
         const int c = 2 * h2 + k;
         *reinterpret_cast<uint4*>(S.q_rope + row * 64 + ((c ^ ((row >> 1) & 3)) * 16)) = x;
       }
+      if (q_range) set_status(p.ws, MLA_STATUS_Q_RANGE);
       ptx::fence_proxy_async_smem();
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
@@ -666,7 +769,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
           const float p0 = ptx::ex2_approx(s[c] - m_use), p1 = ptx::ex2_approx(s[c + 1] - m_use);
           ls0 += p0;
           ls1 += p1;
-          pk[c / 2] = ptx::pack_bf16x2(p0, p1);
+          pk[c / 2] = KV == MLA_KV_BF16 ? ptx::pack_bf16x2(p0, p1) : ptx::pack_f16x2(p0, p1);
         }
         l += ls0 + ls1;
         if (t_idx > 0 && __any_sync(0xffffffffu, grow)) {
@@ -755,27 +858,29 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D view of a bf16 cache: [num_pages * page_size rows, 576 columns], one page per box.
-bool encode_cache_map(CUtensorMap* m, const void* cache, int num_pages, int ps, int box_cols,
+// 2-D view of a bf16 or FP8 cache: [num_pages * page_size rows, 576 columns], one page of
+// rows per box.
+bool encode_cache_map(CUtensorMap* m, const void* cache, int num_pages, int ps, int box_cols, int elem_bytes,
                       CUtensorMapSwizzle sw) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)kDim, (cuuint64_t)num_pages * ps};
-  cuuint64_t strides[1] = {(cuuint64_t)kDim * 2};
+  cuuint64_t strides[1] = {(cuuint64_t)kDim * elem_bytes};
   cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)ps};
   cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(m, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+            const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 }  // namespace
 
 size_t tc_smem_bytes() { return sizeof(tc::Smem) + 1024; }
 
-// Largest number of 2-CTA clusters of the tensor-core kernel that can be co-resident.
+// Largest number of 2-CTA clusters of the tensor-core kernel that can be co-resident (the
+// three cache formats share block size and shared memory).
 int tc_max_clusters() {
-  if (cudaFuncSetAttribute(tc::mla_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)tc_smem_bytes()) != cudaSuccess) {
+  auto kern = tc::mla_decode_tc_kernel<MLA_KV_BF16>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem_bytes()) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -794,24 +899,40 @@ int tc_max_clusters() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, tc::mla_decode_tc_kernel, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
   return n;
 }
 
+template <int KV>
+static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const DecodeParams& p, cudaStream_t stream) {
+  auto kern = tc::mla_decode_tc_kernel<KV>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem_bytes());
+  if (e != cudaSuccess) return e;
+  kern<<<2 * p.workers, tc::kThreads, tc_smem_bytes(), stream>>>(a, b, p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t stream) {
   static_assert(sizeof(tc::Smem) + 1024 <= 227 * 1024, "shared memory budget");
   CUtensorMap tm_lat, tm_rope;
-  if (!encode_cache_map(&tm_lat, p.cache, p.num_pages, p.page_size, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_cache_map(&tm_rope, p.cache, p.num_pages, p.page_size, 32, CU_TENSOR_MAP_SWIZZLE_64B))
-    return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(tc::mla_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)tc_smem_bytes());
-  if (e != cudaSuccess) return e;
-  tc::mla_decode_tc_kernel<<<2 * p.workers, tc::kThreads, tc_smem_bytes(), stream>>>(tm_lat, tm_rope, p);
-  return cudaGetLastError();
+  memset(&tm_lat, 0, sizeof(tm_lat));
+  memset(&tm_rope, 0, sizeof(tm_rope));
+  if (p.kv_dtype == MLA_KV_BF16) {
+    if (!encode_cache_map(&tm_lat, p.cache, p.num_pages, p.page_size, 64, 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_cache_map(&tm_rope, p.cache, p.num_pages, p.page_size, 32, 2, CU_TENSOR_MAP_SWIZZLE_64B))
+      return cudaErrorInvalidValue;
+    return launch_tc<MLA_KV_BF16>(tm_lat, tm_rope, p, stream);
+  }
+  if (p.kv_dtype == MLA_KV_FP8_E4M3) {
+    if (!encode_cache_map(&tm_lat, p.cache, p.num_pages, p.page_size, 256, 1, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_cache_map(&tm_rope, p.cache, p.num_pages, p.page_size, 32, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+    return launch_tc<MLA_KV_FP8_E4M3>(tm_lat, tm_rope, p, stream);
+  }
+  return launch_tc<MLA_KV_NVFP4>(tm_lat, tm_rope, p, stream);
 }
 
 }  // namespace mla
