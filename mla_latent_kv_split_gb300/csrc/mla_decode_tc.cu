@@ -8,8 +8,8 @@
 //   half of V) plus 32 of the 64 rope columns.  The score contraction over 576 columns is
 //   therefore split in two: each CTA computes the partial scores of its 288 columns with
 //   one MMA chain, and the two CTAs exchange the partial fp32 score tiles through
-//   distributed shared memory, so both hold the same full scores, take the same softmax
-//   decisions and produce the same P.  Every cache byte is read from HBM once.
+//   distributed shared memory, so both hold the full scores.  Every cache byte is read
+//   from HBM once.
 //
 // Per CTA, per 64-token tile (TileGym: K = V = KV; tokenspeed: paged cache):
 //   producer warp   TMA-gathers the tile's pages (block table -> page rows) into a
@@ -17,28 +17,34 @@
 //                   swizzle) + 1 box of 64 tokens x 32 rope columns (64-byte swizzle)
 //                   (FP8: the E4M3 bytes of those columns; NVFP4: whole pages, packed
 //                   E2M1 data plus E4M3 scales, into the tail of the stage)
-//   MMA warp        S[128 x 64] = Q[128 x 288] (in TMEM) . K^T       (18 MMAs, K = 16)
-//                   O[128 x 256] += P[128 x 64] (in TMEM) . V[64 x 256] (4 MMAs, N = 256)
-//   sender warps    one warpgroup.  (1) Prepares each landed tile for the MMAs: zeroes the
-//                   rows that are masked (ragged tail, invalid page) so that garbage, even
-//                   NaN, cannot reach P.V, and for FP8 / NVFP4 decodes the raw bytes in place
-//                   into f16 (exact for both formats) in the same swizzled layout.
-//                   (2) Thread = head row: loads the row's 64 partial scores
-//                   from TMEM and pushes them into the peer CTA's exchange buffer with
-//                   asynchronous stores that complete on the peer's mbarrier (the link is
-//                   the slowest path of the exchange, so it gets warps of its own)
-//   softmax warps   two warpgroups; thread (row = head, half h) owns tile columns
-//                   [32h, 32h+32) of its row: loads them from TMEM, waits for the peer's
-//                   partial scores, adds them, combines the row max with the other
-//                   half, runs the online softmax in base 2 with a lazy rescale of O (only
-//                   when the running max grows by more than 8) and writes P (bf16) to
-//                   TMEM; at the end of a work item it normalises its 128 output columns
-//                   and writes the output (or the split partial and its LSE).
+//   MMA warps       one issues S[128 x 64] = Q[128 x 288] (in TMEM) . K^T (18 MMAs, K = 16),
+//                   the other O[128 x 256] += P[128 x 64] (in smem) . V[64 x 256] (4 MMAs, N = 256)
+//   sender warps    one warpgroup.  (1) Prepares landed tiles for the MMAs when needed:
+//                   zeroes the rows that are masked (ragged tail, invalid page) so that
+//                   garbage, even NaN, cannot reach P.V, and for FP8 / NVFP4 decodes the raw
+//                   bytes in place into f16 (exact for both formats) in the same swizzled
+//                   layout.  (2) Thread = head row: loads the row's 64 partial scores from
+//                   TMEM and pushes them (24-bit packed) into the peer CTA's exchange buffer
+//                   with asynchronous stores that complete on the peer's mbarrier.  (3) Loads
+//                   each work item's Q into TMEM (latent) and shared memory (rope).
+//   softmax warps   two warpgroups that take alternate tiles (even / odd), so two tiles are
+//                   in flight; thread = head row, all 64 columns of the tile.  Loads its
+//                   partial scores from TMEM, adds the peer's, takes the row max, and runs
+//                   the online softmax in base 2 with a lazy reference max: the reference
+//                   only moves (and O is rescaled) when a tile's max exceeds it by more than
+//                   8, and the two warpgroups pass it from tile to tile through shared
+//                   memory.  P (bf16 / f16) goes into the exchange slot the partial scores
+//                   arrived in; at the end of a work item both warpgroups normalise O (128
+//                   columns each) and write the output, or the split partial and its LSE.
 //
 // Tensor memory (512 columns): O [0,256) fp32; two score buffers S0 [256,320), S1 [320,384)
-// fp32; Q [384,512) bf16 pairs (this CTA's 256 latent columns).  The 32 rope columns of Q
-// and P (bf16) sit in shared memory, where the rope and P.V MMAs read their A operand, so a
-// score buffer is free again as soon as it has been read.
+// fp32 (S0 holds even tiles, S1 odd tiles); Q [384,512) bf16 pairs (this CTA's 256 latent
+// columns).  The 32 rope columns of Q sit in shared memory, where the rope MMAs read them.
+//
+// Handshakes with the peer CTA: partial scores of tile g go into the peer's exchange slot
+// g&1 (st.async, completing on the peer's x_full[g&1]); the peer's P(g) then overwrites
+// that slot, and the P.V MMAs that read it arrive, through a multicast commit, on the
+// sender's x_empty[g&1]: only then may the sender push the scores of tile g+2.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -57,14 +63,14 @@ constexpr int kTileN = 64;                      // tokens per tile
 constexpr int kLatBox = kTileN * 128;           // 64 rows x 64 bf16 (8 KB)
 constexpr int kRopeBox = kTileN * 64;           // 64 rows x 32 bf16 (4 KB)
 constexpr int kStageBytes = 4 * kLatBox + kRopeBox;  // 36 KB
-// Partial scores cross the cluster as 24-bit floats (fp32 rounded to 15 mantissa bits,
-// relative error <= 2^-16): 4 values in 3 words; one tile = 128 rows x 48 words (24 KB).
-constexpr int kXWordsPerRow = kTileN * 3 / 4;   // 48
-constexpr int kXBytes = 128 * kXWordsPerRow * 4;
+// Partial scores cross the cluster as 24-bit floats (fp32 cut to 15 mantissa bits,
+// relative error < 2^-15): 4 values in 3 words; one row's 64 values = 12 groups of 16
+// bytes, stored [group][row] so that a warp's accesses are contiguous.
+constexpr int kXGroups = 12;
+constexpr int kXBytes = kXGroups * 128 * 16;    // 24 KB per slot
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0, kTmemS = 256, kTmemQ = 384;  // S buffers at kTmemS + 64 * (g & 1)
 constexpr int kQRopeBytes = 128 * 64;  // Q rope: 128 rows x 32 bf16, K-major, 64-byte swizzle
-constexpr int kPBytes = 128 * 128;     // P: 128 rows x 64 tokens 16-bit, K-major, 128-byte swizzle
 // Raw bytes of quantized tiles sit in the tail of a stage and are decoded in place:
 constexpr int kRawFp8 = kStageBytes - kTileN * 288;    // FP8: 256 latent + 32 rope bytes per row
 constexpr int kRawFp8Rope = kRawFp8 + kTileN * 256;
@@ -73,55 +79,41 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;       // log2 units: P stays below 2^8
 
-// warp roles
-constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpRelay = 3, kWarpSender0 = 4, kWarpSoftmax0 = 8;
+// warp roles (warp 3 has none)
+constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpMmaPv = 2, kWarpSender0 = 4, kWarpSoftmax0 = 8;
 constexpr int kSenderThreads = 128;   // warps 4..7
-constexpr int kSoftmaxThreads = 256;  // warps 8..15
+constexpr int kWgThreads = 128;       // one softmax warpgroup: warps 8..11 (even tiles), 12..15 (odd)
+constexpr int kSoftmaxThreads = 256;
 // Registers per thread: the launch gives every thread kLaunchRegs; the control warpgroup
-// (warps 0..3) drops to kCtrlRegs, the sender warpgroup to kSenderRegs, and the two softmax
-// warpgroups rise to kSoftmaxRegs.  The sum must not exceed 512 * kLaunchRegs (65,536).
-constexpr uint32_t kLaunchRegs = 128, kCtrlRegs = 64, kSenderRegs = 128, kSoftmaxRegs = 160;
-static_assert(128 * kCtrlRegs + 128 * kSenderRegs + 256 * kSoftmaxRegs <= 512 * kLaunchRegs,
+// (warps 0..3) drops to ctrl, the sender warpgroup to sender, and the two softmax
+// warpgroups rise to softmax.  The sum must not exceed 512 * kLaunchRegs (65,536); the split
+// follows each cache format's register needs (the senders decode quantized tiles).
+constexpr uint32_t kLaunchRegs = 128;
+template <int KV>
+struct RegSplit;
+template <>
+struct RegSplit<MLA_KV_BF16> {
+  static constexpr uint32_t ctrl = 88, sender = 120, softmax = 152;
+};
+template <>
+struct RegSplit<MLA_KV_FP8_E4M3> {
+  static constexpr uint32_t ctrl = 80, sender = 128, softmax = 152;
+};
+template <>
+struct RegSplit<MLA_KV_NVFP4> {
+  static constexpr uint32_t ctrl = 72, sender = 136, softmax = 152;
+};
+template <int KV>
+constexpr bool reg_split_fits() {
+  return 128 * RegSplit<KV>::ctrl + 128 * RegSplit<KV>::sender + 256 * RegSplit<KV>::softmax <= 512 * kLaunchRegs;
+}
+static_assert(reg_split_fits<MLA_KV_BF16>() && reg_split_fits<MLA_KV_FP8_E4M3>() && reg_split_fits<MLA_KV_NVFP4>(),
               "register split exceeds the launch budget");
-
-struct Bars {
-  uint64_t kv_full[kStages];   // TMA bytes landed
-  uint64_t kv_ready[kStages];  // senders prepared the tile (masked rows zeroed, quantized data decoded)
-  uint64_t deq;                // senders read every raw byte of a tile (before decoding in place)
-  uint64_t kv_empty[kStages];  // P.V of the tile completed: stage reusable
-  uint64_t s_full[2];          // S MMAs of a buffer completed
-  uint64_t s_free[2];          // senders and softmax read a buffer's S
-  uint64_t p_full;             // P written to shared memory (and O rescaled)
-  uint64_t o_done;             // P.V completed
-  uint64_t q_ready;            // Q of the next item in TMEM
-  uint64_t o_free;             // epilogue read O
-  uint64_t x_full[2];          // the peer's partial scores landed in my exchange buffer (tx count)
-  uint64_t x_empty[2];         // peer finished reading its buffer: I may write it again
-  uint64_t x_read[2];          // my softmax warps finished reading my buffer (relayed to the peer)
-  uint64_t mx[2];              // both halves of every row published their tile max
-  uint64_t lsum;               // both halves published their row sums (epilogue)
-  uint64_t mma_final;          // every MMA of this CTA completed
-};
-
-struct Smem {
-  uint8_t stage[kStages][kStageBytes];
-  uint8_t p_tile[kPBytes];  // 1024-byte aligned (swizzle atoms)
-  uint8_t q_rope[kQRopeBytes];
-  uint4 xbuf[2][kXWordsPerRow / 4][128];  // [slot][16-byte group][row], 24-bit packed
-  Bars bars;
-  float mx[2][2][128];   // [tile parity][half][row] partial row maxima
-  float lsum[2][128];    // [half][row] partial row sums
-  uint32_t tmem_base;
-  int abort_flag;
-  int scratch[33];
-  WorkerStart wstart;  // this worker's place in the schedule (the full plan is built in xbuf)
-};
-static_assert(sizeof(PlanSmem) <= 2 * kXBytes, "plan scratch must fit the exchange buffers");
-
-__device__ __forceinline__ Smem& smem_ref(uint8_t* raw) {
-  uintptr_t a = reinterpret_cast<uintptr_t>(raw);
-  a = (a + 1023) & ~uintptr_t(1023);
-  return *reinterpret_cast<Smem*>(a);
+// Moves this warpgroup's per-thread register budget from the launch value to N.
+template <uint32_t N>
+__device__ __forceinline__ void regs_to() {
+  if constexpr (N < kLaunchRegs) ptx::regs_dec<N>();
+  else if constexpr (N > kLaunchRegs) ptx::regs_inc<N>();
 }
 
 // Geometry of one 64-token tile of a work item.
@@ -131,6 +123,50 @@ struct TileInfo {
   bool page_ok[2];
   uint64_t rowmask;  // bit r: row r is a real, visible position
 };
+
+struct Bars {
+  uint64_t kv_full[kStages];   // TMA bytes landed
+  uint64_t kv_ready[kStages];  // tile prepared for the MMAs (quantized: decoded by the senders, every tile;
+                               // bf16: masked rows zeroed by the producer warp, those tiles only)
+  uint64_t deq;                // senders read every raw byte of a tile (before decoding in place)
+  uint64_t kv_empty[kStages];  // P.V of the tile completed: stage reusable
+  uint64_t s_full[2];          // S MMAs of a buffer completed
+  uint64_t s_free[2];          // the senders and the buffer's softmax warpgroup read its S
+  uint64_t p_full[2];          // P written to the exchange slot (and O rescaled)
+  uint64_t o_done[4];          // P.V of tile g completed (barrier g & 3)
+  uint64_t q_ready;            // Q of the next item in TMEM / shared memory
+  uint64_t o_free;             // epilogue read O
+  uint64_t x_full[2];          // the peer's partial scores landed in my exchange slot (tx count)
+  uint64_t x_empty[2];         // the peer's P.V read its slot: I may push the next scores into it
+  uint64_t ep;                 // both softmax warpgroups published their (max, sum) of an item
+  uint64_t mma_final;          // every score MMA of this CTA completed
+  uint64_t mma_final_pv;       // every P.V MMA of this CTA completed
+};
+
+struct Smem {
+  uint8_t stage[kStages][kStageBytes];
+  // [slot][16-byte group][row]: the peer's partial scores of a tile, then (first 16 KB,
+  // 128 rows x 128 bytes, 128-byte swizzle) that tile's P, read by the P.V MMAs
+  uint4 xbuf[2][kXGroups][128];
+  uint8_t q_rope[kQRopeBytes];
+  Bars bars;
+  unsigned long long mchain[128];  // per row: (tile index + 1) << 32 | reference max bits
+  float ep_m[2][2][128];           // [item parity][warpgroup][row] reference max
+  float ep_l[2][2][128];           // [item parity][warpgroup][row] row sum relative to it
+  unsigned long long tmask[kStages];  // rows of the staged tile that are real, visible positions
+  uint32_t tmem_base;
+  int abort_flag;
+  int scratch[33];
+  WorkerStart wstart;  // this worker's place in the schedule (the full plan is built in xbuf)
+};
+static_assert(sizeof(PlanSmem) <= 2 * kXBytes, "plan scratch must fit the exchange buffers");
+static_assert(kXBytes % 1024 == 0 && (kStages * kStageBytes) % 1024 == 0, "P tiles need 1024-byte alignment");
+
+__device__ __forceinline__ Smem& smem_ref(uint8_t* raw) {
+  uintptr_t a = reinterpret_cast<uintptr_t>(raw);
+  a = (a + 1023) & ~uintptr_t(1023);
+  return *reinterpret_cast<Smem*>(a);
+}
 
 __device__ __forceinline__ TileInfo tile_info(const DecodeParams& p, int b, int t0, int tok_hi) {
   TileInfo ti;
@@ -167,53 +203,42 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v, bool& out_of_ran
   return ptx::pack_f16x2(lo, hi);
 }
 
-// fp32 bit pattern rounded to its top 24 bits (sign, exponent, 15 mantissa bits), nearest.
-__device__ __forceinline__ uint32_t round24(uint32_t bits) { return (bits + 0x80u) & 0xFFFFFF00u; }
-// Four fp32 values -> three words holding their rounded top 24 bits.
+// Four fp32 bit patterns -> three words holding their top 24 bits (sign, exponent, 15
+// mantissa bits): w0 = a.hi16 | b.hi16 << 16, w1 = c.hi16 | d.hi16 << 16, w2 = the third
+// bytes of a, b, c, d.  The receiver fills the dropped low byte with another byte of the
+// packet, so the value it gets differs from the sent one by less than 2^-15 relative.
 __device__ __forceinline__ void pack24x4(uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t& w0, uint32_t& w1,
                                          uint32_t& w2) {
-  a = round24(a) >> 8;
-  b = round24(b) >> 8;
-  c = round24(c) >> 8;
-  d = round24(d) >> 8;
-  w0 = a | (b << 24);
-  w1 = (b >> 8) | (c << 16);
-  w2 = (c >> 16) | (d << 8);
+  w0 = __byte_perm(a, b, 0x7632);
+  w1 = __byte_perm(c, d, 0x7632);
+  w2 = __byte_perm(__byte_perm(a, b, 0x0051), __byte_perm(c, d, 0x5100), 0x7610);
 }
 __device__ __forceinline__ void unpack24x4(uint32_t w0, uint32_t w1, uint32_t w2, float& a, float& b, float& c,
                                            float& d) {
-  a = __uint_as_float(w0 << 8);
-  b = __uint_as_float(((w0 >> 24) | (w1 << 8)) << 8);
-  c = __uint_as_float(((w1 >> 16) | (w2 << 16)) << 8);
-  d = __uint_as_float(w2 & 0xFFFFFF00u);
+  a = __uint_as_float(__byte_perm(w0, w2, 0x1044));
+  b = __uint_as_float(__byte_perm(w0, w2, 0x3255));
+  c = __uint_as_float(__byte_perm(w1, w2, 0x1066));
+  d = __uint_as_float(__byte_perm(w1, w2, 0x3277));
 }
 
-// The raw block-table entries of a tile (loaded early, consumed a softmax iteration later).
-struct TilePages {
-  int pg[2];
-};
-__device__ __forceinline__ TilePages tile_pages(const DecodeParams& p, int b, int t0, int tok_hi) {
-  TilePages tp;
-  const int ps = p.page_size;
-#pragma unroll
-  for (int j = 0; j < 2; ++j)
-    tp.pg[j] = (j < kTileN / ps && t0 + j * ps < tok_hi) ? __ldg(p.block_table + (size_t)b * p.max_pages + (t0 + j * ps) / ps)
-                                                          : -1;
-  return tp;
-}
-// Rows [32h, 32h+32) of the tile that are real, visible positions.
-__device__ __forceinline__ uint32_t tile_half_mask(const DecodeParams& p, const TilePages& tp, int t0, int tok_hi,
-                                                   int h) {
-  const int ps = p.page_size;
-  uint64_t m = 0;
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    if (j < kTileN / ps && t0 + j * ps < tok_hi && tp.pg[j] >= 0 && tp.pg[j] < p.num_pages) {
-      const int rows = min(ps, tok_hi - (t0 + j * ps));
-      m |= (rows >= 64 ? ~0ull : ((1ull << rows) - 1)) << (j * ps);
+// Bounded spin until this row's reference-max chain holds tile `g`'s predecessor's entry.
+__device__ __forceinline__ bool chain_wait(const unsigned long long* slot, unsigned g, unsigned long long& v,
+                                           volatile int* abort_flag) {
+  const volatile unsigned long long* vs = slot;
+  v = *vs;
+  if ((unsigned)(v >> 32) == g) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    v = *vs;
+    if ((unsigned)(v >> 32) == g) return true;
+    if ((it & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (ptx::globaltimer_ns() - t0 > 4000000000ull) {
+        *abort_flag = 1;
+        return false;
+      }
     }
   }
-  return (uint32_t)(m >> (32 * h));
 }
 
 // KV: cache format (MLA_KV_BF16 / MLA_KV_FP8_E4M3 / MLA_KV_NVFP4).  The MMAs run in bf16 for a
@@ -240,45 +265,44 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
     __syncthreads();
   }
   const WorkerStart wst = S.wstart;
+  const int n_tiles_total = wst.N;
 
   const uint32_t b_kv_full = ptx::smem_u32(&S.bars.kv_full[0]);
   const uint32_t b_kv_ready = ptx::smem_u32(&S.bars.kv_ready[0]);
   const uint32_t b_kv_empty = ptx::smem_u32(&S.bars.kv_empty[0]);
   const uint32_t b_s_full = ptx::smem_u32(&S.bars.s_full[0]), b_s_free = ptx::smem_u32(&S.bars.s_free[0]);
-  const uint32_t b_p_full = ptx::smem_u32(&S.bars.p_full), b_o_done = ptx::smem_u32(&S.bars.o_done);
+  const uint32_t b_p_full = ptx::smem_u32(&S.bars.p_full[0]), b_o_done = ptx::smem_u32(&S.bars.o_done[0]);
   const uint32_t b_q_ready = ptx::smem_u32(&S.bars.q_ready), b_o_free = ptx::smem_u32(&S.bars.o_free);
   const uint32_t b_x_full = ptx::smem_u32(&S.bars.x_full[0]), b_x_empty = ptx::smem_u32(&S.bars.x_empty[0]);
   const uint32_t b_mma_final = ptx::smem_u32(&S.bars.mma_final);
-  const uint32_t b_mx = ptx::smem_u32(&S.bars.mx[0]), b_lsum = ptx::smem_u32(&S.bars.lsum);
-  const uint32_t b_x_read = ptx::smem_u32(&S.bars.x_read[0]);
+  const uint32_t b_mma_final_pv = ptx::smem_u32(&S.bars.mma_final_pv);
+  const uint32_t b_ep = ptx::smem_u32(&S.bars.ep);
   const uint32_t b_deq = ptx::smem_u32(&S.bars.deq);
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(b_kv_full + 8 * s, 1);
-      ptx::mbar_init(b_kv_ready + 8 * s, kSenderThreads);
+      ptx::mbar_init(b_kv_ready + 8 * s, KV == MLA_KV_BF16 ? 1 : kSenderThreads);
       ptx::mbar_init(b_kv_empty + 8 * s, 1);
     }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(b_s_full + 8 * s, 1);
-      ptx::mbar_init(b_s_free + 8 * s, kSoftmaxThreads + kSenderThreads);
+      ptx::mbar_init(b_s_free + 8 * s, kWgThreads + kSenderThreads);
+      ptx::mbar_init(b_p_full + 8 * s, kWgThreads);
+      ptx::mbar_init(b_x_full + 8 * s, 1);   // one local arrive (expect_tx) + 24 KB of peer bytes
+      ptx::mbar_init(b_x_empty + 8 * s, 1);  // one arrive per use, from the peer's P.V commit
     }
-    ptx::mbar_init(b_p_full, kSoftmaxThreads);
-    ptx::mbar_init(b_o_done, 1);
-    ptx::mbar_init(b_q_ready, kSoftmaxThreads);
+    for (int s = 0; s < 4; ++s) ptx::mbar_init(b_o_done + 8 * s, 1);
+    ptx::mbar_init(b_q_ready, kSenderThreads);
     ptx::mbar_init(b_o_free, kSoftmaxThreads);
-    for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(b_x_full + 8 * s, 1);   // one local arrive (expect_tx) + 32 KB of peer bytes
-      ptx::mbar_init(b_x_empty + 8 * s, 1);  // one arrive per use, from the peer's relay warp
-      ptx::mbar_init(b_mx + 8 * s, kSoftmaxThreads);
-      ptx::mbar_init(b_x_read + 8 * s, kSoftmaxThreads / 32);
-    }
-    ptx::mbar_init(b_lsum, kSoftmaxThreads);
+    ptx::mbar_init(b_ep, kSoftmaxThreads);
     ptx::mbar_init(b_deq, kSenderThreads);
     ptx::mbar_init(b_mma_final, 1);
+    ptx::mbar_init(b_mma_final_pv, 1);
     S.abort_flag = 0;
     ptx::fence_mbar_init_cluster();
   }
+  if (tid < 128) S.mchain[tid] = 0ull;
   if (warp == kWarpMma) {
     ptx::tmem_alloc(ptx::smem_u32(&S.tmem_base), kTmemCols);
     ptx::tmem_relinquish();
@@ -293,28 +317,42 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
   ptx::tc_fence_after();
   const uint32_t tmem = S.tmem_base;
   if (warp == kWarpProducer) {
-    ptx::regs_dec<kCtrlRegs>();
+    regs_to<RegSplit<KV>::ctrl>();
     // ------------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      int g = 0;
-      for_each_item_cursor(p, wst, worker, [&](const WorkItem& it) {
-        const int b = it.u / p.q_len;
-        // Let the first item's queries reach the memory system before this CTA's burst of
-        // cache loads (otherwise they queue behind every SM's initial TMA traffic).
-        if (g == 0 && !ptx::mbar_wait(b_q_ready, 0, abort_flag)) return;
-        for (int t0 = it.tok_lo; t0 < it.tok_hi; t0 += kTileN, ++g) {
-          if (*abort_flag) return;
-          const int st = g % kStages;
-          if (g >= kStages && !ptx::mbar_wait(b_kv_empty + 8 * st, ((g / kStages) - 1) & 1, abort_flag)) return;
-          const TileInfo ti = tile_info(p, b, t0, it.tok_hi);
-          const uint32_t page_bytes = KV == MLA_KV_BF16 ? (uint32_t)p.page_size * (4 * 128 + 64)
-                                    : KV == MLA_KV_FP8_E4M3 ? (uint32_t)p.page_size * 288
-                                                            : (uint32_t)p.page_size * 324;
+    // Lane 0 issues the loads.  For a bf16 tile with masked rows (ragged tail, invalid page)
+    // the whole warp waits for it to land and zeroes those rows, so that garbage, even NaN,
+    // cannot reach P.V, then releases it to the score MMAs (kv_ready).
+    const bool leader = lane == 0;
+    const uint32_t page_bytes = KV == MLA_KV_BF16 ? (uint32_t)p.page_size * (4 * 128 + 64)
+                              : KV == MLA_KV_FP8_E4M3 ? (uint32_t)p.page_size * 288
+                                                      : (uint32_t)p.page_size * 324;
+    int g = 0;
+    bool dead = false;
+    ItemCursor cur = item_cursor(p, wst, worker);
+    WorkItem it;
+    while (!dead && next_item(p, n_tiles_total, cur, it)) {
+      const int b = it.u / p.q_len;
+      // Let the first item's queries reach the memory system before this CTA's burst of
+      // cache loads (otherwise they queue behind every SM's initial TMA traffic).
+      if (g == 0 && !ptx::mbar_wait(b_q_ready, 0, abort_flag)) break;
+      TileInfo ti_next = tile_info(p, b, it.tok_lo, it.tok_hi);
+      for (int t0 = it.tok_lo; t0 < it.tok_hi; t0 += kTileN, ++g) {
+        // this tile's block-table entries were read one tile earlier, the next tile's are
+        // read now, before waiting for the stage
+        const TileInfo ti = ti_next;
+        if (t0 + kTileN < it.tok_hi) ti_next = tile_info(p, b, t0 + kTileN, it.tok_hi);
+        const int st = g % kStages;
+        if (g >= kStages && !ptx::mbar_wait(b_kv_empty + 8 * st, ((g / kStages) - 1) & 1, abort_flag)) {
+          dead = true;
+          break;
+        }
+        if (leader) {
           uint32_t bytes = 0;
           for (int j = 0; j < ti.npages; ++j) {
             if (ti.page_ok[j]) bytes += page_bytes;
             else set_status(p.ws, MLA_STATUS_PAGE_OUT_OF_RANGE);
           }
+          S.tmask[st] = ti.rowmask;  // published by the arrive below
           ptx::mbar_arrive_expect_tx(b_kv_full + 8 * st, bytes);
           const uint32_t dst = ptx::smem_u32(S.stage[st]);
           for (int j = 0; j < ti.npages; ++j) {
@@ -336,130 +374,149 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
             }
           }
         }
-      });
-      // loads still in flight after an abort must land before the CTA exits
+        if (KV == MLA_KV_BF16 && ti.rowmask != ~0ull) {
+          if (!ptx::mbar_wait(b_kv_full + 8 * st, (g / kStages) & 1, abort_flag)) {
+            dead = true;
+            break;
+          }
+          // a masked row: 4 latent boxes x 128 bytes + 64 rope bytes, zeroed whole
+          uint8_t* base = S.stage[st];
+#pragma unroll 1
+          for (int r = 0; r < kTileN; ++r) {
+            if ((ti.rowmask >> r) & 1ull) continue;
+            for (int c = lane; c < 36; c += 32)
+              *reinterpret_cast<uint4*>(c < 32 ? base + (c >> 3) * kLatBox + r * 128 + (c & 7) * 16
+                                               : base + 4 * kLatBox + r * 64 + (c - 32) * 16) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (leader) ptx::mbar_arrive(b_kv_ready + 8 * st);
+        }
+      }
+    }
+    // loads still in flight after an abort must land before the CTA exits
+    if (leader) {
       for (int k = 1; k <= kStages && g - k >= 0; ++k) {
         const int gg = g - k;
         ptx::mbar_wait(b_kv_full + 8 * (gg % kStages), (gg / kStages) & 1, abort_flag, false, 100000000ull);
       }
     }
   } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------------ MMA issuer
-    ptx::regs_dec<kCtrlRegs>();
-    // Per item, an event loop: the score MMAs of the next tile are issued as soon as its
-    // cache tile has landed and the softmax has read the previous scores, independently
-    // of the P.V of earlier tiles, which are issued whenever their P is ready.
+    // ------------------------------------------------------------------ score MMA issuer
+    // Issuing a chain of MMAs blocks this thread while the tensor pipe takes them in, so the
+    // score MMAs and the P.V MMAs have issuers of their own: a P.V whose P is ready never
+    // waits behind the issue of the next tile's scores.
+    regs_to<RegSplit<KV>::ctrl>();
     if (lane == 0) {
       constexpr uint32_t ab = KV == MLA_KV_BF16 ? 1u : 0u;                 // bf16 / f16 operands
       constexpr uint32_t idesc_s = ptx::idesc_f16(ab, 0, 128, kTileN);  // K-major B (cache rows)
-      constexpr uint32_t idesc_o = ptx::idesc_f16(ab, 1, 128, 256);     // MN-major B (V columns)
       const uint32_t stage0 = ptx::smem_u32(S.stage[0]);
       // base descriptors of stage 0; stage st adds st * kStageBytes to the address field
       const uint64_t kdesc0 = ptx::umma_desc(stage0, 16, 1024, 2);               // K rows, 128 B swizzle
       const uint64_t rdesc0 = ptx::umma_desc(stage0 + 4 * kLatBox, 16, 512, 4);  // rope rows, 64 B swizzle
-      const uint64_t vdesc0 = ptx::umma_desc(stage0, kLatBox, 1024, 2);          // V, MN-major
       const uint64_t qdesc0 = ptx::umma_desc(ptx::smem_u32(S.q_rope), 16, 512, 4);
-      const uint64_t pdesc0 = ptx::umma_desc(ptx::smem_u32(S.p_tile), 16, 1024, 2);  // P, K-major
       int g = 0, n_item = 0;
+      uint32_t fixpar = 0;  // bf16: per-stage phase of kv_ready (it completes on tiles with masked rows only)
       bool dead = false;
-      for_each_item_cursor(p, wst, worker, [&](const WorkItem& it) {
-        if (dead) return;
-        if (!ptx::mbar_wait(b_q_ready, n_item & 1, abort_flag)) { dead = true; return; }
+      ItemCursor cur = item_cursor(p, wst, worker);
+      WorkItem it;
+      while (!dead && next_item(p, n_tiles_total, cur, it)) {
+        if (!ptx::mbar_wait(b_q_ready, n_item & 1, abort_flag)) break;
         ptx::tc_fence_after();
         const int nt = (it.tok_hi - it.tok_lo + kTileN - 1) / kTileN;
-        const int g0 = g;
-        int ts = 0, tp = 0;  // next tile whose S / P.V is to be issued
-        bool o_free_ok = n_item == 0;
-        uint64_t t_idle = 0;
-        while (tp < nt) {
-          bool progressed = false;
-          // P.V first: its completion is what frees a cache stage for the next load
-          if (tp < ts) {
-            const int gp = g0 + tp;
-            if (!o_free_ok) o_free_ok = ptx::mbar_test(b_o_free, (n_item - 1) & 1);
-            if (o_free_ok && ptx::mbar_test(b_p_full, gp & 1)) {
-              ptx::tc_fence_after();
-              const uint64_t vdesc = vdesc0 + (uint64_t)((gp % kStages) * (kStageBytes >> 4));
-#pragma unroll
-              for (int k = 0; k < kTileN / 16; ++k)  // 16 tokens = 2 KB of V rows, 32 B of P rows
-                ptx::mma_ss(tmem + kTmemO, pdesc0 + (uint64_t)(k * 2), vdesc + (uint64_t)(k * (2048 >> 4)), idesc_o,
-                            (tp == 0 && k == 0) ? 0u : 1u);
-              ptx::mma_commit(b_o_done);
-              ptx::mma_commit(b_kv_empty + 8 * (gp % kStages));
-              ++tp;
-              progressed = true;
+        for (int t = 0; t < nt; ++t, ++g) {
+          const int st = g % kStages;
+          if (KV == MLA_KV_BF16) {
+            if (!ptx::mbar_wait(b_kv_full + 8 * st, (g / kStages) & 1, abort_flag)) { dead = true; break; }
+            if (S.tmask[st] != ~0ull) {
+              if (!ptx::mbar_wait(b_kv_ready + 8 * st, (fixpar >> st) & 1u, abort_flag)) { dead = true; break; }
+              fixpar ^= 1u << st;
             }
-          }
-          if (ts < nt) {
-            const int gs = g0 + ts, st = gs % kStages;
-            // buffer gs&1 is free once the senders and the softmax have read S(gs-2)
-            if (ptx::mbar_test(b_kv_ready + 8 * st, (gs / kStages) & 1) &&
-                       (gs < 2 || ptx::mbar_test(b_s_free + 8 * (gs & 1), ((gs >> 1) - 1) & 1))) {
-              const uint32_t d_s = tmem + kTmemS + 64 * (gs & 1);
-              ptx::tc_fence_after();
-              // Descriptors advance by constant offsets (16-byte units): 32 B per K step in a
-              // 128-byte swizzle row, one 8 KB box per 64 latent columns.
-              const uint64_t kdesc = kdesc0 + (uint64_t)(st * (kStageBytes >> 4));
-              const uint64_t rdesc = rdesc0 + (uint64_t)(st * (kStageBytes >> 4));
-#pragma unroll
-              for (int k = 0; k < 16; ++k)  // 256 latent columns: 4 boxes x 4 steps of 16
-                ptx::mma_ts(d_s, tmem + kTmemQ + 8 * k, kdesc + (uint64_t)((k >> 2) * (kLatBox >> 4) + (k & 3) * 2),
-                            idesc_s, k > 0 ? 1u : 0u);
-#pragma unroll
-              for (int k = 0; k < 2; ++k)  // 32 rope columns (64-byte swizzle), Q rope from smem
-                ptx::mma_ss(d_s, qdesc0 + (uint64_t)(k * 2), rdesc + (uint64_t)(k * 2), idesc_s, 1u);
-              ptx::mma_commit(b_s_full + 8 * (gs & 1));
-              ++ts;
-              progressed = true;
-            }
-          }
-          if (progressed) {
-            t_idle = 0;
           } else {
-            const uint64_t now = ptx::globaltimer_ns();
-            if (t_idle == 0) {
-              t_idle = now;
-            } else if (*abort_flag || now - t_idle > 4000000000ull) {
-              *abort_flag = 1;
-              dead = true;
-              return;
-            }
+            if (!ptx::mbar_wait(b_kv_ready + 8 * st, (g / kStages) & 1, abort_flag)) { dead = true; break; }
           }
+          // buffer g&1 is free once the senders and its softmax warpgroup have read S(g-2)
+          if (g >= 2 && !ptx::mbar_wait(b_s_free + 8 * (g & 1), ((g >> 1) - 1) & 1, abort_flag)) { dead = true; break; }
+          ptx::tc_fence_after();
+          const uint32_t d_s = tmem + kTmemS + 64 * (g & 1);
+          // Descriptors advance by constant offsets (16-byte units): 32 B per K step in a
+          // 128-byte swizzle row, one 8 KB box per 64 latent columns.
+          const uint64_t kdesc = kdesc0 + (uint64_t)(st * (kStageBytes >> 4));
+          const uint64_t rdesc = rdesc0 + (uint64_t)(st * (kStageBytes >> 4));
+#pragma unroll
+          for (int k = 0; k < 16; ++k)  // 256 latent columns: 4 boxes x 4 steps of 16
+            ptx::mma_ts(d_s, tmem + kTmemQ + 8 * k, kdesc + (uint64_t)((k >> 2) * (kLatBox >> 4) + (k & 3) * 2),
+                        idesc_s, k > 0 ? 1u : 0u);
+#pragma unroll
+          for (int k = 0; k < 2; ++k)  // 32 rope columns (64-byte swizzle), Q rope from smem
+            ptx::mma_ss(d_s, qdesc0 + (uint64_t)(k * 2), rdesc + (uint64_t)(k * 2), idesc_s, 1u);
+          ptx::mma_commit(b_s_full + 8 * (g & 1));
         }
-        g += nt;
         ++n_item;
-      });
+      }
       ptx::mma_commit(b_mma_final);
       ptx::mbar_wait(b_mma_final, 0, abort_flag, false, 100000000ull);
     }
+  } else if (warp == kWarpMmaPv) {
+    // ------------------------------------------------------------------ P.V MMA issuer
+    regs_to<RegSplit<KV>::ctrl>();
+    if (lane == 0) {
+      constexpr uint32_t ab = KV == MLA_KV_BF16 ? 1u : 0u;
+      constexpr uint32_t idesc_o = ptx::idesc_f16(ab, 1, 128, 256);  // MN-major B (V columns)
+      const uint64_t vdesc0 = ptx::umma_desc(ptx::smem_u32(S.stage[0]), kLatBox, 1024, 2);        // V, MN-major
+      const uint64_t pdesc0 = ptx::umma_desc(ptx::smem_u32(&S.xbuf[0][0][0]), 16, 1024, 2);  // P, K-major
+      const uint16_t peer_mask = (uint16_t)(1u << peer);
+      int g = 0, n_item = 0;
+      bool dead = false;
+      ItemCursor cur = item_cursor(p, wst, worker);
+      WorkItem it;
+      while (!dead && next_item(p, n_tiles_total, cur, it)) {
+        const int nt = (it.tok_hi - it.tok_lo + kTileN - 1) / kTileN;
+        for (int t = 0; t < nt; ++t, ++g) {
+          if (!ptx::mbar_wait(b_p_full + 8 * (g & 1), (g >> 1) & 1, abort_flag)) { dead = true; break; }
+          // the item's first P.V overwrites O: the previous item's epilogue must have read it
+          if (t == 0 && n_item > 0 && !ptx::mbar_wait(b_o_free, (n_item - 1) & 1, abort_flag)) { dead = true; break; }
+          ptx::tc_fence_after();
+          const uint64_t vdesc = vdesc0 + (uint64_t)((g % kStages) * (kStageBytes >> 4));
+          const uint64_t pdesc = pdesc0 + (uint64_t)((g & 1) * (kXBytes >> 4));
+#pragma unroll
+          for (int k = 0; k < kTileN / 16; ++k)  // 16 tokens = 2 KB of V rows, 32 B of P rows
+            ptx::mma_ss(tmem + kTmemO, pdesc + (uint64_t)(k * 2), vdesc + (uint64_t)(k * (2048 >> 4)), idesc_o,
+                        (t == 0 && k == 0) ? 0u : 1u);
+          ptx::mma_commit(b_o_done + 8 * (g & 3));
+          ptx::mma_commit(b_kv_empty + 8 * (g % kStages));
+          ptx::mma_commit_multicast(b_x_empty + 8 * (g & 1), peer_mask);
+        }
+        ++n_item;
+      }
+      ptx::mma_commit(b_mma_final_pv);
+      ptx::mbar_wait(b_mma_final_pv, 0, abort_flag, false, 100000000ull);
+    }
   } else if (warp >= kWarpSender0 && warp < kWarpSoftmax0) {
-    // ------------------------------------------------------------------ score sender
-    ptx::regs_dec<kSenderRegs>();
+    // ------------------------------------------------------------------ senders
+    regs_to<RegSplit<KV>::sender>();
     const int q = warp & 3;
     const int row = 32 * q + lane;
-    const uint32_t t_s0 = tmem + ((uint32_t)(32 * q) << 16) + kTmemS;
+    const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+    const uint32_t t_s0 = tmem + lane_off + kTmemS, t_q = tmem + lane_off + kTmemQ;
     const uint32_t x_peer = ptx::mapa(ptx::smem_u32(&S.xbuf[0][0][0]), peer);
     const uint32_t bx_full_peer = ptx::mapa(b_x_full, peer);
     const int tq = (warp - kWarpSender0) * 32 + lane;  // 0..127
     const int pr = tq >> 1, phf = tq & 1;              // prepare: row and half-row (18 chunks of 8)
 
-    // (1) Tile k has landed: zero masked rows; decode FP8 / NVFP4 bytes in place to f16.
-    auto prepare = [&](int k, const TileInfo& ti) -> bool {
+    // (1) Quantized caches: tile k has landed; decode its FP8 / NVFP4 bytes in place to f16
+    // (masked rows become zeros).
+    auto prepare = [&](int k) -> bool {
       const int st = k % kStages;
       if (!ptx::mbar_wait(b_kv_full + 8 * st, (k / kStages) & 1, abort_flag)) return false;
       uint8_t* base = S.stage[st];
-      const bool valid = (ti.rowmask >> pr) & 1ull;
+      const bool valid = (S.tmask[st] >> pr) & 1ull;
       // destination of 16-byte chunk c (8 values) of row pr in the swizzled operand layout
       auto chunk_ptr = [&](int c) -> uint4* {
         return reinterpret_cast<uint4*>(c < 32 ? base + (c >> 3) * kLatBox + pr * 128 + (((c & 7) ^ (pr & 7)) * 16)
                                               : base + 4 * kLatBox + pr * 64 + ((((c - 32) ^ ((pr >> 1) & 3))) * 16));
       };
-      if (KV == MLA_KV_BF16) {
-        if (!valid) {
-#pragma unroll 1
-          for (int c = 18 * phf; c < 18 * phf + 18; ++c) *chunk_ptr(c) = make_uint4(0u, 0u, 0u, 0u);
-        }
-      } else {
+      {
         // every raw byte this thread needs -> registers, then (after all senders did the
         // same) the decoded values over the same stage
         uint32_t raw[18][2];
@@ -521,6 +578,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       ptx::tc_fence_before();
       ptx::mbar_arrive(b_s_free + 8 * (k & 1));
       const int slot = k & 1, use = k >> 1;
+      // the peer's P.V(k-2) has read the slot (its P) before the next scores go in
       if (use >= 1 && !ptx::mbar_wait(b_x_empty + 8 * slot, (use - 1) & 1, abort_flag, true)) return false;
       const uint32_t xp = x_peer + (uint32_t)slot * kXBytes + (uint32_t)row * 16;
       const uint32_t bar = bx_full_peer + 8 * slot;
@@ -540,65 +598,50 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       return true;
     };
 
-    // Tile k is prepared one step before tile k-1's scores are sent.
-    int g = 0;
-    bool dead = false;
-    for_each_item_cursor(p, wst, worker, [&](const WorkItem& it) {
-      const int b = it.u / p.q_len;
-      for (int t0 = it.tok_lo; t0 < it.tok_hi; t0 += kTileN, ++g) {
-        if (dead || *abort_flag) return;
-        const TileInfo ti = tile_info(p, b, t0, it.tok_hi);
-        if (!prepare(g, ti) || (g > 0 && !send(g - 1))) { dead = true; return; }
-      }
-    });
-    if (!dead && g > 0) send(g - 1);
-  } else if (warp >= kWarpSoftmax0) {
-    // ------------------------------------------------------------------ softmax + epilogue
-    ptx::regs_inc<kSoftmaxRegs>();
-    const int sw = warp - kWarpSoftmax0;  // 0..7
-    const int h2 = sw >> 2;               // half: tile columns [32*h2, +32), O columns [128*h2, +128)
-    const int q = warp & 3;               // TMEM lane quadrant this warp may access
-    const int row = 32 * q + lane;        // head
-    const uint32_t lane_off = (uint32_t)(32 * q) << 16;
-    const uint32_t t_s0 = tmem + lane_off + kTmemS;  // + 64 * buffer
-    const uint32_t t_o = tmem + lane_off + kTmemO + 128 * h2, t_q = tmem + lane_off + kTmemQ;
-    const float scale_log2 = p.sm_scale * p.kv_scale * kLog2e;
-
-    // Q of one work item -> TMEM: this thread's 128 latent columns and 16 rope columns
-    auto load_q = [&](const WorkItem& it) {
-      const int b = it.u / p.q_len, i = it.u % p.q_len;
-      uint32_t v[32];
+    // (3) Q of one work item: this row's 256 latent columns -> TMEM, 32 rope columns ->
+    // shared memory (64-byte swizzled K-major layout: chunk c of row r sits at chunk
+    // position c ^ ((r >> 1) & 3) of the row's 64 bytes).
+    auto q_row = [&](const WorkItem& w) -> size_t {
+      const int b = w.u / p.q_len, i = w.u % p.q_len;
+      return ((size_t)b * p.q_len + i) * p.H + (row < p.H ? row : 0);
+    };
+    auto load_q = [&](const WorkItem& w) {
       const bool real = row < p.H;
-      const size_t qrow = ((size_t)b * p.q_len + i) * p.H + (real ? row : 0);
-      const uint4* qn = reinterpret_cast<const uint4*>(p.q_nope + qrow * kLatent + 256 * cr + 128 * h2);
+      const size_t qrow = q_row(w);
+      const uint4* qn = reinterpret_cast<const uint4*>(p.q_nope + qrow * kLatent + 256 * cr);
+      const uint4* qp = reinterpret_cast<const uint4*>(p.q_pe + qrow * kRope + 32 * cr);
       bool q_range = false;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int half = 0; half < 2; ++half) {
+        uint4 x[16];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint4 x = real ? __ldg(qn + c * 8 + k) : make_uint4(0u, 0u, 0u, 0u);
-          v[4 * k] = x.x; v[4 * k + 1] = x.y; v[4 * k + 2] = x.z; v[4 * k + 3] = x.w;
-        }
-        if (KV != MLA_KV_BF16) {
+        for (int k = 0; k < 16; ++k) x[k] = real ? __ldg(qn + 16 * half + k) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-          for (int k = 0; k < 32; ++k) v[k] = bf16x2_to_f16x2(v[k], q_range);
+        for (int c = 0; c < 2; ++c) {
+          uint32_t v[32];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            v[4 * k] = x[8 * c + k].x;
+            v[4 * k + 1] = x[8 * c + k].y;
+            v[4 * k + 2] = x[8 * c + k].z;
+            v[4 * k + 3] = x[8 * c + k].w;
+          }
+          if (KV != MLA_KV_BF16) {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] = bf16x2_to_f16x2(v[k], q_range);
+          }
+          ptx::tmem_st32(t_q + 64 * half + 32 * c, v);
         }
-        ptx::tmem_st32(t_q + 64 * h2 + 32 * c, v);
       }
-      // rope: this thread's 16 values = 2 of the row's four 16-byte chunks, stored in the
-      // 64-byte-swizzled K-major layout the rope MMAs read (chunk c of row r sits at
-      // chunk position c ^ ((r >> 1) & 3) of the row's 64 bytes)
-      const uint4* qp = reinterpret_cast<const uint4*>(p.q_pe + qrow * kRope + 32 * cr + 16 * h2);
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        uint4 x = real ? __ldg(qp + k) : make_uint4(0u, 0u, 0u, 0u);
+      for (int c = 0; c < 4; ++c) {
+        uint4 x = real ? __ldg(qp + c) : make_uint4(0u, 0u, 0u, 0u);
         if (KV != MLA_KV_BF16) {
           x.x = bf16x2_to_f16x2(x.x, q_range);
           x.y = bf16x2_to_f16x2(x.y, q_range);
           x.z = bf16x2_to_f16x2(x.z, q_range);
           x.w = bf16x2_to_f16x2(x.w, q_range);
         }
-        const int c = 2 * h2 + k;
         *reinterpret_cast<uint4*>(S.q_rope + row * 64 + ((c ^ ((row >> 1) & 3)) * 16)) = x;
       }
       if (q_range) set_status(p.ws, MLA_STATUS_Q_RANGE);
@@ -607,34 +650,224 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       ptx::tc_fence_before();
       ptx::mbar_arrive(b_q_ready);
     };
+    // pull the next item's queries into L2 while this item runs
+    auto prefetch_q = [&](const WorkItem& w) {
+      if (row >= p.H) return;
+      const size_t qrow = q_row(w);
+      const uint8_t* qn = reinterpret_cast<const uint8_t*>(p.q_nope + qrow * kLatent + 256 * cr);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) ptx::prefetch_l2(qn + 128 * k);
+      ptx::prefetch_l2(p.q_pe + qrow * kRope + 32 * cr);
+    };
 
-    // Epilogue of a finished item: O / l for this thread's 128 columns, and the LSE.
-    // P.V completions are awaited in order (od = next tile not yet awaited); P(g) is only
-    // handed over after P.V(g-1) completed, so o_done is never two phases ahead of a wait.
-    int od = 0;
+    // Per tile g: quantized caches decode tile g first (its S MMAs wait for it), then send
+    // tile g-1's scores.  An item's Q is loaded once the previous item's last scores have been
+    // read out of TMEM.
+    int g = 0;
+    bool dead = false;
+    ItemCursor cur = item_cursor(p, wst, worker);
+    WorkItem it;
+    while (!dead && next_item(p, n_tiles_total, cur, it)) {
+      {
+        ItemCursor look = cur;
+        WorkItem nx;
+        if (next_item(p, n_tiles_total, look, nx)) prefetch_q(nx);
+      }
+      if (g == 0) load_q(it);  // the producer waits for it before its first cache load
+      for (int t0 = it.tok_lo; t0 < it.tok_hi; t0 += kTileN, ++g) {
+        if (*abort_flag) { dead = true; break; }
+        if (KV != MLA_KV_BF16 && !prepare(g)) { dead = true; break; }
+        if (g > 0 && !send(g - 1)) { dead = true; break; }
+        if (t0 == it.tok_lo && g > 0) load_q(it);
+      }
+    }
+    if (!dead && g > 0 && send(g - 1)) {
+      // the peer's last two P.V commits land on this CTA's x_empty: take them before exit
+      for (int k = max(0, g - 2); k < g; ++k)
+        if (!ptx::mbar_wait(b_x_empty + 8 * (k & 1), (k >> 1) & 1, abort_flag, true)) break;
+    }
+  } else if (warp >= kWarpSoftmax0) {
+    // ------------------------------------------------------------------ softmax + epilogue
+    regs_to<RegSplit<KV>::softmax>();
+    const int wg = (warp - kWarpSoftmax0) >> 2;  // tiles g with g & 1 == wg; O columns [128 wg, +128)
+    const int q = warp & 3;                       // TMEM lane quadrant this warp may access
+    const int row = 32 * q + lane;                // head
+    const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+    const uint32_t t_s = tmem + lane_off + kTmemS + 64 * wg;
+    const uint32_t t_o = tmem + lane_off + kTmemO;
+    const float scale_log2 = p.sm_scale * p.kv_scale * kLog2e;
+    const uint32_t b_pf = b_p_full + 8 * wg, b_xf = b_x_full + 8 * wg, b_sf = b_s_full + 8 * wg;
+    const uint32_t b_sfree = b_s_free + 8 * wg;
+    uint8_t* const pslot = reinterpret_cast<uint8_t*>(&S.xbuf[wg][0][0]);
+    unsigned long long* const chain = &S.mchain[row];
+
+    // P.V completions: o_done[k & 3] completes once per P.V(k), k = j, j + 4, ...  Every P.V
+    // up to pv_known is known to be complete, and the waits below are only ever for
+    // P.V(k) with k <= pv_known + 4, so the barrier's previous phase (P.V(k-4)) is complete
+    // and its next one (P.V(k+4)) cannot complete before this thread moves on: a parity
+    // wait never confuses two phases.
+    int pv_known = -1;
     auto wait_pv = [&](int k) -> bool {
-      for (; od <= k; ++od)
-        if (!ptx::mbar_wait(b_o_done, od & 1, abort_flag)) return false;
+      if (k <= pv_known) return true;
+      if (!ptx::mbar_wait(b_o_done + 8 * (k & 3), (k >> 2) & 1, abort_flag)) return false;
+      pv_known = k;
       return true;
     };
-    auto epilogue = [&](const WorkItem& it, float m_ref, float l_half, int g_last, int n_ep) -> bool {
-      S.lsum[h2][row] = l_half;
-      ptx::mbar_arrive(b_lsum);
-      if (!wait_pv(g_last)) return false;
-      if (!ptx::mbar_wait(b_lsum, n_ep & 1, abort_flag)) return false;
+
+    int g = 0, n_item = 0;
+    bool dead = false;
+    ItemCursor cur = item_cursor(p, wst, worker);
+    WorkItem it;
+    while (!dead && next_item(p, n_tiles_total, cur, it)) {
+      const int b = it.u / p.q_len;
+      const int nt = (it.tok_hi - it.tok_lo + kTileN - 1) / kTileN;
+      const int g0 = g;
+      float m_own = -INFINITY, l_own = 0.f;  // this warpgroup's row sum and the reference it is relative to
+      int t_idx = (g0 & 1) == wg ? 0 : 1;     // this warpgroup's first tile of the item
+      for (; t_idx < nt; t_idx += 2) {
+        const int gg = g0 + t_idx;
+        // ---- own partial scores
+        float s[64];
+        if (!ptx::mbar_wait(b_sf, (gg >> 1) & 1, abort_flag)) { dead = true; break; }
+        ptx::tc_fence_after();
+        {
+          uint32_t r0[32], r1[32];
+          ptx::tmem_ld32(t_s, r0);
+          ptx::tmem_ld32(t_s + 32, r1);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            s[k] = __uint_as_float(r0[k]);
+            s[32 + k] = __uint_as_float(r1[k]);
+          }
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(b_sfree);
+        // ---- the peer's partial scores (pushed by its senders)
+        if (q == 0 && lane == 0) ptx::mbar_arrive_expect_tx(b_xf, kXBytes);
+        if (!ptx::mbar_wait(b_xf, (gg >> 1) & 1, abort_flag, true)) { dead = true; break; }
+        // the peer pushed these only after P.V(gg-2) of this CTA had read the slot
+        if (gg - 2 > pv_known) pv_known = gg - 2;
+        uint32_t xw[48];
+#pragma unroll
+        for (int k = 0; k < kXGroups; ++k) {
+          const uint4 v = S.xbuf[wg][k][row];
+          xw[4 * k] = v.x;
+          xw[4 * k + 1] = v.y;
+          xw[4 * k + 2] = v.z;
+          xw[4 * k + 3] = v.w;
+        }
+        // every row of the slot has been read: P may overwrite it
+        ptx::named_bar_sync(1 + wg, kWgThreads);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          float a, b2, c, d;
+          unpack24x4(xw[3 * j], xw[3 * j + 1], xw[3 * j + 2], a, b2, c, d);
+          s[4 * j] += a;
+          s[4 * j + 1] += b2;
+          s[4 * j + 2] += c;
+          s[4 * j + 3] += d;
+        }
+        // ---- mask (tail tiles only), row max (raw units; the scale is positive)
+        // the producer published the tile's row mask with the tile's kv_full phase, which
+        // completed before this tile's scores (and cannot move on before P(gg) is handed over)
+        const int st = gg % kStages;
+        if (!ptx::mbar_wait(b_kv_full + 8 * st, (gg / kStages) & 1, abort_flag)) { dead = true; break; }
+        const uint64_t mask = S.tmask[st];
+        if (mask != ~0ull) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) s[c] = ((mask >> c) & 1ull) ? s[c] : -INFINITY;
+        }
+        float m4[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+        for (int c = 4; c < 64; c += 4) {
+          m4[0] = fmaxf(m4[0], s[c]);
+          m4[1] = fmaxf(m4[1], s[c + 1]);
+          m4[2] = fmaxf(m4[2], s[c + 2]);
+          m4[3] = fmaxf(m4[3], s[c + 3]);
+        }
+        const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * scale_log2;
+        // ---- reference max: take the previous tile's, move it when this tile exceeds it by > 8
+        float m_prev = -INFINITY;
+        if (gg > 0) {
+          unsigned long long v;
+          if (!chain_wait(chain, (unsigned)gg, v, abort_flag)) { dead = true; break; }
+          if (t_idx > 0) m_prev = __uint_as_float((uint32_t)v);
+        }
+        const bool grow = mt > m_prev + kRescaleThreshold;
+        const float m_new = grow ? mt : m_prev;
+        *reinterpret_cast<volatile unsigned long long*>(chain) =
+            ((unsigned long long)(unsigned)(gg + 1) << 32) | __float_as_uint(m_new);
+        // this warpgroup's running sum follows the reference
+        if (m_new != m_own) {
+          if (l_own != 0.f) l_own *= ptx::ex2_approx(m_own - m_new);
+          m_own = m_new;
+        }
+        const float m_use = m_new == -INFINITY ? 0.f : m_new;
+        uint32_t pk[32];
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          const float p0 = ptx::ex2_approx(fmaf(s[c], scale_log2, -m_use));
+          const float p1 = ptx::ex2_approx(fmaf(s[c + 1], scale_log2, -m_use));
+          ls[(c >> 1) & 3] += p0 + p1;
+          // bf16: round half up on the bit pattern (p is finite and non-negative)
+          pk[c / 2] = KV == MLA_KV_BF16 ? __byte_perm(__float_as_uint(p0) + 0x8000u, __float_as_uint(p1) + 0x8000u, 0x7632)
+                                        : ptx::pack_f16x2(p0, p1);
+        }
+        l_own += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        // P(gg) -> the slot.  Row r, 16-byte chunk c (8 tokens) sits at chunk position
+        // c ^ (r & 7) of the row's 128 bytes (the 128-byte swizzle the P.V MMAs read).
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(pslot + row * 128 + ((c ^ (row & 7)) * 16)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        if (t_idx > 0 && __any_sync(0xffffffffu, grow)) {
+          // O (all 256 columns of these rows) moves to the new reference once P.V(gg-1) is
+          // done, before P(gg) is handed over
+          if (!wait_pv(gg - 1)) { dead = true; break; }
+          ptx::tc_fence_after();
+          const float a = grow ? ptx::ex2_approx(m_prev - m_new) : 1.f;
+#pragma unroll 1
+          for (int c = 0; c < 16; ++c) {
+            uint32_t r[16];
+            ptx::tmem_ld16(t_o + 16 * c, r);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < 16; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * a);
+            ptx::tmem_st16(t_o + 16 * c, r);
+          }
+          ptx::tmem_st_wait();
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(b_pf);
+      }
+      if (dead) break;
+      g = g0 + nt;
+      // ---- epilogue: O / l for this warpgroup's 128 columns, and the LSE
+      const int par = n_item & 1;
+      S.ep_m[par][wg][row] = m_own;
+      S.ep_l[par][wg][row] = l_own;
+      ptx::mbar_arrive(b_ep);
+      if (!wait_pv(g - 1)) { dead = true; break; }
+      if (!ptx::mbar_wait(b_ep, par, abort_flag)) { dead = true; break; }
       ptx::tc_fence_after();
-      const float l = S.lsum[0][row] + S.lsum[1][row];
-      const int b = it.u / p.q_len, i = it.u % p.q_len;
+      const float ma = S.ep_m[par][0][row], mb = S.ep_m[par][1][row];
+      const float la = S.ep_l[par][0][row], lb = S.ep_l[par][1][row];
+      const float m_fin = fmaxf(ma, mb);
+      const float l = (la > 0.f ? la * ptx::ex2_approx(ma - m_fin) : 0.f) + (lb > 0.f ? lb * ptx::ex2_approx(mb - m_fin) : 0.f);
+      const int i = it.u % p.q_len;
       const bool real = row < p.H;
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      const float lse_v = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+      const float lse_v = l > 0.f ? (m_fin + __log2f(l)) * kLn2 : -INFINITY;
       const float oscale = inv * p.kv_scale;
       const size_t orow = ((size_t)b * p.q_len + i) * p.H + (real ? row : 0);
-      const int col0 = 256 * (int)cr + 128 * h2;
+      const int col0 = 256 * (int)cr + 128 * wg;
       const bool direct = it.slot < 0, partial = it.slot >= 0 && it.slot < p.slots_cap;
       for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
-        ptx::tmem_ld32(t_o + 32 * c, r);
+        ptx::tmem_ld32(t_o + 128 * wg + 32 * c, r);
         ptx::tmem_ld_wait();
         if (real && direct) {
           uint4* dst = reinterpret_cast<uint4*>(p.out + orow * kLatent + col0 + 32 * c);
@@ -657,7 +890,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
                                  __uint_as_float(r[4 * k + 2]) * oscale, __uint_as_float(r[4 * k + 3]) * oscale);
         }
       }
-      if (real && cr == 0 && h2 == 0) {
+      if (real && cr == 0 && wg == 0) {
         if (direct) {
           if (p.lse) p.lse[orow] = lse_v;
         } else if (partial) {
@@ -666,166 +899,10 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(b_o_free);
-      return true;
-    };
-
-    int g = 0, n_ep = 0;
-    bool dead = false, have_prev = false;
-    WorkItem prev{};
-    float prev_m = -INFINITY, prev_l = 0.f;
-    int prev_g_last = -1;
-    for_each_item_cursor(p, wst, worker, [&](const WorkItem& it) {
-      if (dead) return;
-      // Order: this item's Q (every S of the previous item has been read, so the Q region
-      // is free), then the previous item's epilogue, so the MMA warp can already run this
-      // item's first score tile while the epilogue drains O.
-      load_q(it);
-      if (have_prev) {
-        if (!epilogue(prev, prev_m, prev_l, prev_g_last, n_ep)) { dead = true; return; }
-        ++n_ep;
-      }
-      const int b = it.u / p.q_len;
-      const int nt = (it.tok_hi - it.tok_lo + kTileN - 1) / kTileN;
-      float m_ref = -INFINITY, l = 0.f;
-      TilePages pages = tile_pages(p, b, it.tok_lo, it.tok_hi);
-      for (int t_idx = 0; t_idx < nt; ++t_idx, ++g) {
-        const int t0 = it.tok_lo + t_idx * kTileN;
-        const TilePages pg_cur = pages;
-        if (t_idx + 1 < nt) pages = tile_pages(p, b, t0 + kTileN, it.tok_hi);  // next tile, consumed next iteration
-        // ---- own partial scores of this half
-        float cur[32];
-        const uint32_t t_s = t_s0 + 64 * (g & 1);
-        if (!ptx::mbar_wait(b_s_full + 8 * (g & 1), (g >> 1) & 1, abort_flag)) { dead = true; return; }
-        ptx::tc_fence_after();
-        {
-          uint32_t r[32];
-          ptx::tmem_ld32(t_s + 32 * h2, r);
-          ptx::tmem_ld_wait();
-#pragma unroll
-          for (int k = 0; k < 32; ++k) cur[k] = __uint_as_float(round24(r[k]));  // as the peer receives it
-        }
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(b_s_free + 8 * (g & 1));
-        // ---- the peer's partial scores (pushed by its sender warps)
-        const int slot = g & 1, use = g >> 1;
-        if (sw == 0 && lane == 0) ptx::mbar_arrive_expect_tx(b_x_full + 8 * slot, kXBytes);
-        if (!ptx::mbar_wait(b_x_full + 8 * slot, use & 1, abort_flag, true)) { dead = true; return; }
-        float* s = cur;  // full scores of this tile, in place
-        uint32_t xw[24];
-#pragma unroll
-        for (int k = 0; k < 6; ++k) {  // this half's 32 values = 24 words = 6 groups of 4 words
-          const uint4 v = S.xbuf[slot][6 * h2 + k][row];
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) xw[4 * k + j] = w[j];
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          float a, b2, c, d;
-          unpack24x4(xw[3 * j], xw[3 * j + 1], xw[3 * j + 2], a, b2, c, d);
-          s[4 * j] += a;
-          s[4 * j + 1] += b2;
-          s[4 * j + 2] += c;
-          s[4 * j + 3] += d;
-        }
-        // The peer may overwrite this buffer once every warp has read it.  The release to
-        // the peer is done by the relay warp: a release here would also wait for this
-        // thread's asynchronous stores of the next tile, still in flight.
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive_relaxed(b_x_read + 8 * slot);
-        // ---- scale, mask (tail tiles only), row max over both halves
-        const uint32_t mymask = tile_half_mask(p, pg_cur, t0, it.tok_hi, h2);
-        float mh = -INFINITY;
-        if (mymask == 0xffffffffu) {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            s[c] *= scale_log2;
-            mh = fmaxf(mh, s[c]);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            s[c] = ((mymask >> c) & 1u) ? s[c] * scale_log2 : -INFINITY;
-            mh = fmaxf(mh, s[c]);
-          }
-        }
-        S.mx[g & 1][h2][row] = mh;
-        ptx::mbar_arrive(b_mx + 8 * (g & 1));
-        if (!ptx::mbar_wait(b_mx + 8 * (g & 1), (g >> 1) & 1, abort_flag)) { dead = true; return; }
-        const float mt = fmaxf(mh, S.mx[g & 1][h2 ^ 1][row]);
-        // ---- online softmax (base 2), lazy rescale; both halves take identical decisions
-        float alpha = 1.f;
-        const bool grow = mt > m_ref + kRescaleThreshold;
-        if (grow) {
-          alpha = ptx::ex2_approx(m_ref - mt);  // m_ref = -inf -> 0
-          l *= alpha;
-          m_ref = mt;
-        }
-        const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-        uint32_t pk[16];
-        float ls0 = 0.f, ls1 = 0.f;
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const float p0 = ptx::ex2_approx(s[c] - m_use), p1 = ptx::ex2_approx(s[c + 1] - m_use);
-          ls0 += p0;
-          ls1 += p1;
-          pk[c / 2] = KV == MLA_KV_BF16 ? ptx::pack_bf16x2(p0, p1) : ptx::pack_f16x2(p0, p1);
-        }
-        l += ls0 + ls1;
-        if (t_idx > 0 && __any_sync(0xffffffffu, grow)) {
-          // rescale this thread's 128 columns of O once P.V of the previous tile is done
-          if (!wait_pv(g - 1)) { dead = true; return; }
-          ptx::tc_fence_after();
-          {
-            const float a = grow ? alpha : 1.f;
-            for (int c = 0; c < 8; ++c) {
-              uint32_t r[16];
-              ptx::tmem_ld16(t_o + 16 * c, r);
-              ptx::tmem_ld_wait();
-#pragma unroll
-              for (int k = 0; k < 16; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * a);
-              ptx::tmem_st16(t_o + 16 * c, r);
-            }
-          }
-        }
-        // P(g) -> shared memory once P.V(g-1) has consumed P(g-1).  Row r, 16-byte chunk c
-        // (8 tokens) sits at chunk position c ^ (r & 7) of the row's 128 bytes (the 128-byte
-        // swizzle the P.V MMAs read).
-        if (t_idx > 0 && !wait_pv(g - 1)) { dead = true; return; }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int chunk = 4 * h2 + c;
-          *reinterpret_cast<uint4*>(S.p_tile + row * 128 + ((chunk ^ (row & 7)) * 16)) =
-              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        }
-        ptx::fence_proxy_async_smem();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(b_p_full);
-      }
-      have_prev = true;
-      prev = it;
-      prev_m = m_ref;
-      prev_l = l;
-      prev_g_last = g - 1;
-    });
-    if (have_prev && !dead) epilogue(prev, prev_m, prev_l, prev_g_last, n_ep);
-  } else {
-    // ------------------------------------------------------------------ exchange relay
-    // Forwards "my softmax warps have read exchange buffer s" to the peer CTA (the
-    // peer's x_empty), with cluster-scope release, from a thread with no stores in flight.
-    ptx::regs_dec<kCtrlRegs>();
-    if (warp == kWarpRelay && lane == 0) {
-      const uint32_t bx_empty_peer = ptx::mapa(b_x_empty, peer);
-      int g = 0;
-      for_each_item_cursor(p, wst, worker, [&](const WorkItem& it) {
-        for (int t0 = it.tok_lo; t0 < it.tok_hi; t0 += kTileN, ++g) {
-          if (*abort_flag) return;
-          const int slot = g & 1, use = g >> 1;
-          if (!ptx::mbar_wait(b_x_read + 8 * slot, use & 1, abort_flag)) return;
-          ptx::mbar_arrive_remote(bx_empty_peer + 8 * slot);
-        }
-      });
+      ++n_item;
     }
+  } else {
+    regs_to<RegSplit<KV>::ctrl>();  // warp 3: no role
   }
 
   // ------------------------------------------------------------------ teardown

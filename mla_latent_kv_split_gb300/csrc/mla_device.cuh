@@ -268,55 +268,79 @@ __device__ __forceinline__ int unit_visible_dev(const DecodeParams& p, int u) {
   return unit_visible(clamp_seq_len(__ldg(p.seq_lens + b), p.max_pages, p.page_size), p.q_len, i);
 }
 
-// Same items, same order as for_each_item, walking units from the worker's start.
-template <class F>
-__device__ inline void for_each_item_cursor(const DecodeParams& p, const WorkerStart& w, int c, F&& f) {
-  const int N = w.N;
-  if (N <= 0) return;
+// Worker c's items one at a time, in for_each_item's order, walking units from the worker's
+// start and reading only seq_lens.  A copy of a cursor looks ahead without disturbing it.
+struct ItemCursor {
+  int u, sacc, j, ib, c;
+  long long tb, t, e;
+  bool live;
+};
+
+__device__ inline ItemCursor item_cursor(const DecodeParams& p, const WorkerStart& w, int c) {
+  ItemCursor k{};
+  k.c = c;
+  k.live = w.N > 0;
+  k.u = w.u0;
+  k.sacc = w.slot0;
+  if (!k.live) return k;
   if (p.num_splits > 0) {
-    const int C = p.workers;
-    int u = w.u0, ib = w.base0, sacc = w.slot0;
-    for (int j = c; j < N; j += C) {
-      int vis, tiles, parts, span;
-      for (;;) {
-        vis = unit_visible_dev(p, u);
-        tiles = cdiv_i(vis, kTile);
-        span = forced_span_tiles(vis, p.num_splits);
-        parts = tiles ? cdiv_i(tiles, span) : 0;
-        if (ib + parts > j) break;
-        sacc += parts > 1 ? parts : 0;
-        ib += parts;
-        ++u;
-      }
-      const int k = j - ib;
-      const int lo = k * span, hi = min((k + 1) * span, tiles);
-      f(WorkItem{u, lo * kTile, min(hi * kTile, vis), parts > 1 ? sacc + k : -1});
-    }
+    k.ib = w.base0;
+    k.j = c;
   } else {
-    const int Ca = active_workers(N, p.workers);
-    if (c >= Ca) return;
-    const long long s = worker_begin(c, N, Ca), e = worker_begin(c + 1, N, Ca);
-    if (s >= e) return;
-    int u = w.u0, sacc = w.slot0;
-    long long tb = w.base0, t = s;
-    while (t < e) {
-      const int vis = unit_visible_dev(p, u);
-      const int tiles = cdiv_i(vis, kTile);
-      const long long te = tb + tiles;
-      const int parts = tiles ? worker_of(te - 1, N, Ca) - worker_of(tb, N, Ca) + 1 : 0;
-      if (te > t) {
-        const int lo = (int)(t - tb), hi = (int)(min(e, te) - tb);
-        const int slot = parts > 1 ? sacc + (c - worker_of(tb, N, Ca)) : -1;
-        f(WorkItem{u, lo * kTile, min(hi * kTile, vis), slot});
-        t = min(e, te);
-      }
-      if (t >= te) {
-        sacc += parts > 1 ? parts : 0;
-        tb = te;
-        ++u;
-      }
+    const int Ca = active_workers(w.N, p.workers);
+    if (c >= Ca) {
+      k.live = false;
+      return k;
     }
+    k.t = worker_begin(c, w.N, Ca);
+    k.e = worker_begin(c + 1, w.N, Ca);
+    k.tb = w.base0;
+    if (k.t >= k.e) k.live = false;
   }
+  return k;
+}
+
+__device__ inline bool next_item(const DecodeParams& p, int N, ItemCursor& k, WorkItem& it) {
+  if (!k.live) return false;
+  if (p.num_splits > 0) {
+    if (k.j >= N) return false;
+    int vis, tiles, parts, span;
+    for (;;) {
+      vis = unit_visible_dev(p, k.u);
+      tiles = cdiv_i(vis, kTile);
+      span = forced_span_tiles(vis, p.num_splits);
+      parts = tiles ? cdiv_i(tiles, span) : 0;
+      if (k.ib + parts > k.j) break;
+      k.sacc += parts > 1 ? parts : 0;
+      k.ib += parts;
+      ++k.u;
+    }
+    const int q = k.j - k.ib;
+    const int lo = q * span, hi = min((q + 1) * span, tiles);
+    it = WorkItem{k.u, lo * kTile, min(hi * kTile, vis), parts > 1 ? k.sacc + q : -1};
+    k.j += p.workers;
+    return true;
+  }
+  const int Ca = active_workers(N, p.workers);
+  while (k.t < k.e) {
+    const int vis = unit_visible_dev(p, k.u);
+    const int tiles = cdiv_i(vis, kTile);
+    const long long te = k.tb + tiles;
+    const int parts = tiles ? worker_of(te - 1, N, Ca) - worker_of(k.tb, N, Ca) + 1 : 0;
+    const bool emit = te > k.t;
+    if (emit) {
+      const int lo = (int)(k.t - k.tb), hi = (int)(min(k.e, te) - k.tb);
+      it = WorkItem{k.u, lo * kTile, min(hi * kTile, vis), parts > 1 ? k.sacc + (k.c - worker_of(k.tb, N, Ca)) : -1};
+      k.t = min(k.e, te);
+    }
+    if (k.t >= te) {
+      k.sacc += parts > 1 ? parts : 0;
+      k.tb = te;
+      ++k.u;
+    }
+    if (emit) return true;
+  }
+  return false;
 }
 
 }  // namespace mla
