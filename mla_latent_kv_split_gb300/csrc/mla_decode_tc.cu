@@ -78,9 +78,14 @@ constexpr int kRawFp4 = kStageBytes - kTileN * 324;    // NVFP4: whole pages (28
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;       // log2 units: P stays below 2^8
+// Work items reach the roles through a ring in shared memory written by the item warp; a
+// slot is free again once every reader took it: the producer warp, the two MMA issuers,
+// the 4 sender warps and the 8 softmax warps.
+constexpr int kItemRing = 16;
+constexpr uint32_t kItemReaders = 15;
 
-// warp roles (warp 3 has none)
-constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpMmaPv = 2, kWarpSender0 = 4, kWarpSoftmax0 = 8;
+// warp roles
+constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpMmaPv = 2, kWarpItems = 3, kWarpSender0 = 4, kWarpSoftmax0 = 8;
 constexpr int kSenderThreads = 128;   // warps 4..7
 constexpr int kWgThreads = 128;       // one softmax warpgroup: warps 8..11 (even tiles), 12..15 (odd)
 constexpr int kSoftmaxThreads = 256;
@@ -141,6 +146,8 @@ struct Bars {
   uint64_t ep;                 // both softmax warpgroups published their (max, sum) of an item
   uint64_t mma_final;          // every score MMA of this CTA completed
   uint64_t mma_final_pv;       // every P.V MMA of this CTA completed
+  uint64_t item_full[kItemRing];   // ring slot holds the next work item
+  uint64_t item_empty[kItemRing];  // every reader took the slot's item
 };
 
 struct Smem {
@@ -148,9 +155,13 @@ struct Smem {
   // [slot][16-byte group][row]: the peer's partial scores of a tile, then (first 16 KB,
   // 128 rows x 128 bytes, 128-byte swizzle) that tile's P, read by the P.V MMAs
   uint4 xbuf[2][kXGroups][128];
+  // epilogue staging, per softmax warp: one 16-column chunk of its 32 rows as two 16-row
+  // boxes (fp32: 64-byte rows, 64-byte swizzle; bf16: 32-byte rows, 32-byte swizzle)
+  uint8_t ostage[8][2048];
   uint8_t q_rope[kQRopeBytes];
   Bars bars;
   unsigned long long mchain[128];  // per row: (tile index + 1) << 32 | reference max bits
+  int4 items[kItemRing];           // work items {u, tok_lo, tok_hi, slot}; tok_hi < 0 ends the list
   float ep_m[2][2][128];           // [item parity][warpgroup][row] reference max
   float ep_l[2][2][128];           // [item parity][warpgroup][row] row sum relative to it
   unsigned long long tmask[kStages];  // rows of the staged tile that are real, visible positions
@@ -168,27 +179,26 @@ __device__ __forceinline__ Smem& smem_ref(uint8_t* raw) {
   return *reinterpret_cast<Smem*>(a);
 }
 
+// (page_size is 32 or 64: one or two pages per tile)
 __device__ __forceinline__ TileInfo tile_info(const DecodeParams& p, int b, int t0, int tok_hi) {
   TileInfo ti;
-  const int ps = p.page_size;
-  const int per = kTileN / ps;  // 1 or 2 pages per tile
+  const bool two = p.page_size == 32;
+  const int shift = two ? 5 : 6;
+  const int* row = p.block_table + (size_t)b * p.max_pages;
   ti.npages = 0;
   ti.rowmask = 0;
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     ti.page[j] = -1;
     ti.page_ok[j] = false;
-    if (j < per && t0 + j * ps < tok_hi) {
-      const int lp = (t0 + j * ps) / ps;
-      const int pg = __ldg(p.block_table + (size_t)b * p.max_pages + lp);
+    const int tj = t0 + (j << shift);
+    if ((j == 0 || two) && tj < tok_hi) {
+      const int pg = __ldg(row + (tj >> shift));
       ti.page[j] = pg;
       ti.page_ok[j] = pg >= 0 && pg < p.num_pages;
       ti.npages = j + 1;
-      const int rows = min(ps, tok_hi - (t0 + j * ps));
-      if (ti.page_ok[j]) {
-        const uint64_t m = rows >= 64 ? ~0ull : ((1ull << rows) - 1);
-        ti.rowmask |= m << (j * ps);
-      }
+      const int rows = min(p.page_size, tok_hi - tj);
+      if (ti.page_ok[j]) ti.rowmask |= (rows >= 64 ? ~0ull : ((1ull << rows) - 1)) << (j << shift);
     }
   }
   return ti;
@@ -241,11 +251,26 @@ __device__ __forceinline__ bool chain_wait(const unsigned long long* slot, unsig
   }
 }
 
+// Takes work item k from the ring (every reader takes every item, in order): waits for it,
+// copies it and frees the slot.  Called by a whole warp (one arrive, after all lanes copied)
+// or by a single thread.  Returns 1 for an item, 0 at the end of the list, -1 on abort.
+__device__ __forceinline__ int item_take(const int4* ring, uint32_t b_full, uint32_t b_empty, int k,
+                                         volatile int* abort_flag, WorkItem& it, bool whole_warp) {
+  const int s = k % kItemRing;
+  if (!ptx::mbar_wait(b_full + 8 * s, (uint32_t)(k / kItemRing) & 1u, abort_flag)) return -1;
+  const int4 v = ring[s];
+  if (whole_warp) __syncwarp();
+  if (!whole_warp || (threadIdx.x & 31) == 0) ptx::mbar_arrive(b_empty + 8 * s);
+  it = WorkItem{v.x, v.y, v.z, v.w};
+  return v.z >= 0 ? 1 : 0;
+}
+
 // KV: cache format (MLA_KV_BF16 / MLA_KV_FP8_E4M3 / MLA_KV_NVFP4).  The MMAs run in bf16 for a
 // bf16 cache and in f16 for the quantized ones (E4M3 and E2M1 x E4M3 are exact in f16).
 template <int KV>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope,
+                     const __grid_constant__ CUtensorMap tm_out, const __grid_constant__ CUtensorMap tm_part,
                      const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   Smem& S = smem_ref(smem_raw);
@@ -278,6 +303,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
   const uint32_t b_mma_final_pv = ptx::smem_u32(&S.bars.mma_final_pv);
   const uint32_t b_ep = ptx::smem_u32(&S.bars.ep);
   const uint32_t b_deq = ptx::smem_u32(&S.bars.deq);
+  const uint32_t b_item_full = ptx::smem_u32(&S.bars.item_full[0]), b_item_empty = ptx::smem_u32(&S.bars.item_empty[0]);
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -299,6 +325,10 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
     ptx::mbar_init(b_deq, kSenderThreads);
     ptx::mbar_init(b_mma_final, 1);
     ptx::mbar_init(b_mma_final_pv, 1);
+    for (int s = 0; s < kItemRing; ++s) {
+      ptx::mbar_init(b_item_full + 8 * s, 1);
+      ptx::mbar_init(b_item_empty + 8 * s, kItemReaders);
+    }
     S.abort_flag = 0;
     ptx::fence_mbar_init_cluster();
   }
@@ -328,9 +358,13 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
                                                       : (uint32_t)p.page_size * 324;
     int g = 0;
     bool dead = false;
-    ItemCursor cur = item_cursor(p, wst, worker);
     WorkItem it;
-    while (!dead && next_item(p, n_tiles_total, cur, it)) {
+    for (int k_item = 0;; ++k_item) {
+      const int got = item_take(S.items, b_item_full, b_item_empty, k_item, abort_flag, it, true);
+      if (got <= 0) {
+        dead = got < 0;
+        break;
+      }
       const int b = it.u / p.q_len;
       // Let the first item's queries reach the memory system before this CTA's burst of
       // cache loads (otherwise they queue behind every SM's initial TMA traffic).
@@ -418,9 +452,9 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       int g = 0, n_item = 0;
       uint32_t fixpar = 0;  // bf16: per-stage phase of kv_ready (it completes on tiles with masked rows only)
       bool dead = false;
-      ItemCursor cur = item_cursor(p, wst, worker);
       WorkItem it;
-      while (!dead && next_item(p, n_tiles_total, cur, it)) {
+      for (int k_item = 0; !dead; ++k_item) {
+        if (item_take(S.items, b_item_full, b_item_empty, k_item, abort_flag, it, false) <= 0) break;
         if (!ptx::mbar_wait(b_q_ready, n_item & 1, abort_flag)) break;
         ptx::tc_fence_after();
         const int nt = (it.tok_hi - it.tok_lo + kTileN - 1) / kTileN;
@@ -468,9 +502,9 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       const uint16_t peer_mask = (uint16_t)(1u << peer);
       int g = 0, n_item = 0;
       bool dead = false;
-      ItemCursor cur = item_cursor(p, wst, worker);
       WorkItem it;
-      while (!dead && next_item(p, n_tiles_total, cur, it)) {
+      for (int k_item = 0; !dead; ++k_item) {
+        if (item_take(S.items, b_item_full, b_item_empty, k_item, abort_flag, it, false) <= 0) break;
         const int nt = (it.tok_hi - it.tok_lo + kTileN - 1) / kTileN;
         for (int t = 0; t < nt; ++t, ++g) {
           if (!ptx::mbar_wait(b_p_full + 8 * (g & 1), (g >> 1) & 1, abort_flag)) { dead = true; break; }
@@ -611,7 +645,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       const uint4* qn = reinterpret_cast<const uint4*>(p.q_nope + qrow * kLatent + 256 * cr);
       const uint4* qp = reinterpret_cast<const uint4*>(p.q_pe + qrow * kRope + 32 * cr);
       bool q_range = false;
-#pragma unroll
+#pragma unroll 1
       for (int half = 0; half < 2; ++half) {
         uint4 x[16];
 #pragma unroll
@@ -650,28 +684,17 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       ptx::tc_fence_before();
       ptx::mbar_arrive(b_q_ready);
     };
-    // pull the next item's queries into L2 while this item runs
-    auto prefetch_q = [&](const WorkItem& w) {
-      if (row >= p.H) return;
-      const size_t qrow = q_row(w);
-      const uint8_t* qn = reinterpret_cast<const uint8_t*>(p.q_nope + qrow * kLatent + 256 * cr);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) ptx::prefetch_l2(qn + 128 * k);
-      ptx::prefetch_l2(p.q_pe + qrow * kRope + 32 * cr);
-    };
-
     // Per tile g: quantized caches decode tile g first (its S MMAs wait for it), then send
     // tile g-1's scores.  An item's Q is loaded once the previous item's last scores have been
     // read out of TMEM.
     int g = 0;
     bool dead = false;
-    ItemCursor cur = item_cursor(p, wst, worker);
     WorkItem it;
-    while (!dead && next_item(p, n_tiles_total, cur, it)) {
-      {
-        ItemCursor look = cur;
-        WorkItem nx;
-        if (next_item(p, n_tiles_total, look, nx)) prefetch_q(nx);
+    for (int k_item = 0; !dead; ++k_item) {
+      const int got = item_take(S.items, b_item_full, b_item_empty, k_item, abort_flag, it, true);
+      if (got <= 0) {
+        dead = got < 0;
+        break;
       }
       if (g == 0) load_q(it);  // the producer waits for it before its first cache load
       for (int t0 = it.tok_lo; t0 < it.tok_hi; t0 += kTileN, ++g) {
@@ -689,7 +712,8 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
   } else if (warp >= kWarpSoftmax0) {
     // ------------------------------------------------------------------ softmax + epilogue
     regs_to<RegSplit<KV>::softmax>();
-    const int wg = (warp - kWarpSoftmax0) >> 2;  // tiles g with g & 1 == wg; O columns [128 wg, +128)
+    const int sw = warp - kWarpSoftmax0;        // 0..7
+    const int wg = sw >> 2;                      // tiles g with g & 1 == wg; O columns [128 wg, +128)
     const int q = warp & 3;                       // TMEM lane quadrant this warp may access
     const int row = 32 * q + lane;                // head
     const uint32_t lane_off = (uint32_t)(32 * q) << 16;
@@ -716,9 +740,9 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
 
     int g = 0, n_item = 0;
     bool dead = false;
-    ItemCursor cur = item_cursor(p, wst, worker);
     WorkItem it;
-    while (!dead && next_item(p, n_tiles_total, cur, it)) {
+    for (int k_item = 0; !dead; ++k_item) {
+      if (item_take(S.items, b_item_full, b_item_empty, k_item, abort_flag, it, true) <= 0) break;
       const int b = it.u / p.q_len;
       const int nt = (it.tok_hi - it.tok_lo + kTileN - 1) / kTileN;
       const int g0 = g;
@@ -863,31 +887,48 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       const float lse_v = l > 0.f ? (m_fin + __log2f(l)) * kLn2 : -INFINITY;
       const float oscale = inv * p.kv_scale;
       const size_t orow = ((size_t)b * p.q_len + i) * p.H + (real ? row : 0);
-      const int col0 = 256 * (int)cr + 128 * wg;
       const bool direct = it.slot < 0, partial = it.slot >= 0 && it.slot < p.slots_cap;
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        ptx::tmem_ld32(t_o + 128 * wg + 32 * c, r);
+      // O leaves through shared memory and TMA tensor stores (16 columns x 16 rows per box):
+      // scattered per-thread global stores would cost one memory request per row.
+      const CUtensorMap* tmap = direct ? &tm_out : &tm_part;
+      const int row0 = (direct ? it.u : it.slot) * p.H + 32 * q;
+      const bool store = direct || partial;
+      uint8_t* const stg = S.ostage[sw];
+      const uint32_t stg_a = ptx::smem_u32(stg);
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        uint32_t r[16];
+        ptx::tmem_ld16(t_o + 128 * wg + 16 * c, r);
         ptx::tmem_ld_wait();
-        if (real && direct) {
-          uint4* dst = reinterpret_cast<uint4*>(p.out + orow * kLatent + col0 + 32 * c);
+        // the previous chunk's stores (this item's or the last item's) have read the staging buffer
+        if (lane == 0) ptx::bulk_wait_read();
+        __syncwarp();
+        const int br = lane & 15;
+        if (direct) {
+          uint8_t* rowp = stg + (lane >> 4) * 512 + br * 32;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            uint4 w;
-            w.x = ptx::pack_bf16x2(__uint_as_float(r[8 * k + 0]) * oscale, __uint_as_float(r[8 * k + 1]) * oscale);
-            w.y = ptx::pack_bf16x2(__uint_as_float(r[8 * k + 2]) * oscale, __uint_as_float(r[8 * k + 3]) * oscale);
-            w.z = ptx::pack_bf16x2(__uint_as_float(r[8 * k + 4]) * oscale, __uint_as_float(r[8 * k + 5]) * oscale);
-            w.w = ptx::pack_bf16x2(__uint_as_float(r[8 * k + 6]) * oscale, __uint_as_float(r[8 * k + 7]) * oscale);
-            dst[k] = w;
-          }
+          for (int k = 0; k < 2; ++k)
+            *reinterpret_cast<uint4*>(rowp + ((k ^ ((br >> 2) & 1)) * 16)) =
+                make_uint4(ptx::pack_bf16x2(__uint_as_float(r[8 * k + 0]) * oscale, __uint_as_float(r[8 * k + 1]) * oscale),
+                           ptx::pack_bf16x2(__uint_as_float(r[8 * k + 2]) * oscale, __uint_as_float(r[8 * k + 3]) * oscale),
+                           ptx::pack_bf16x2(__uint_as_float(r[8 * k + 4]) * oscale, __uint_as_float(r[8 * k + 5]) * oscale),
+                           ptx::pack_bf16x2(__uint_as_float(r[8 * k + 6]) * oscale, __uint_as_float(r[8 * k + 7]) * oscale));
+        } else {
+          uint8_t* rowp = stg + (lane >> 4) * 1024 + br * 64;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            *reinterpret_cast<float4*>(rowp + ((k ^ ((br >> 1) & 3)) * 16)) =
+                make_float4(__uint_as_float(r[4 * k]) * oscale, __uint_as_float(r[4 * k + 1]) * oscale,
+                            __uint_as_float(r[4 * k + 2]) * oscale, __uint_as_float(r[4 * k + 3]) * oscale);
         }
-        if (real && partial) {
-          float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.ws + partial_o_offset()) +
-                                                  ((size_t)it.slot * p.H + row) * kLatent + col0 + 32 * c);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && store) {
+          const int x = 256 * (int)cr + 128 * wg + 16 * c;
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            dst[k] = make_float4(__uint_as_float(r[4 * k]) * oscale, __uint_as_float(r[4 * k + 1]) * oscale,
-                                 __uint_as_float(r[4 * k + 2]) * oscale, __uint_as_float(r[4 * k + 3]) * oscale);
+          for (int h = 0; h < 2; ++h)
+            if (32 * q + 16 * h < p.H) ptx::tma_store_2d(tmap, stg_a + h * (direct ? 512 : 1024), x, row0 + 16 * h);
+          ptx::bulk_commit();
         }
       }
       if (real && cr == 0 && wg == 0) {
@@ -901,10 +942,31 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       ptx::mbar_arrive(b_o_free);
       ++n_item;
     }
-  } else {
-    regs_to<RegSplit<KV>::ctrl>();  // warp 3: no role
+  } else if (warp == kWarpItems) {
+    // ------------------------------------------------------------------ work items
+    // Walks this worker's items once, publishes them to the ring, and asks L2 for each
+    // item's query rows ahead of the senders' loads.
+    regs_to<RegSplit<KV>::ctrl>();
+    if (lane == 0) {
+      ItemCursor cur = item_cursor(p, wst, worker);
+      WorkItem nx;
+      for (int k = 0;; ++k) {
+        const bool more = next_item(p, n_tiles_total, cur, nx);
+        const int s = k % kItemRing;
+        if (k >= kItemRing && !ptx::mbar_wait(b_item_empty + 8 * s, (uint32_t)((k / kItemRing) - 1) & 1u, abort_flag))
+          break;
+        if (more && cr == 0) {
+          ptx::bulk_prefetch_l2(p.q_nope + (size_t)nx.u * p.H * kLatent, (uint32_t)p.H * kLatent * 2);
+          ptx::bulk_prefetch_l2(p.q_pe + (size_t)nx.u * p.H * kRope, (uint32_t)p.H * kRope * 2);
+        }
+        S.items[s] = more ? make_int4(nx.u, nx.tok_lo, nx.tok_hi, nx.slot) : make_int4(0, 0, -1, -1);
+        ptx::mbar_arrive(b_item_full + 8 * s);
+        if (!more) break;
+      }
+    }
   }
 
+  if (warp >= kWarpSoftmax0 && lane == 0) ptx::bulk_wait_all();  // epilogue stores done before exit
   // ------------------------------------------------------------------ teardown
   ptx::tc_fence_before();
   __syncthreads();
@@ -949,6 +1011,18 @@ bool encode_cache_map(CUtensorMap* m, const void* cache, int num_pages, int ps, 
             const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+// Row-major [rows, 512] output tensor (bf16 or fp32), boxes of 16 columns x 16 rows.
+bool encode_rows_map(CUtensorMap* m, const void* base, size_t rows, int elem_bytes, CUtensorMapSwizzle sw) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rows == 0) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)kLatent, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kLatent * elem_bytes};
+  cuuint32_t box[2] = {16, 16};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 }  // namespace
 
 size_t tc_smem_bytes() { return sizeof(tc::Smem) + 1024; }
@@ -984,32 +1058,42 @@ int tc_max_clusters() {
 }
 
 template <int KV>
-static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const DecodeParams& p, cudaStream_t stream) {
+static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o, const CUtensorMap& w,
+                             const DecodeParams& p, cudaStream_t stream) {
   auto kern = tc::mla_decode_tc_kernel<KV>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem_bytes());
   if (e != cudaSuccess) return e;
-  kern<<<2 * p.workers, tc::kThreads, tc_smem_bytes(), stream>>>(a, b, p);
+  kern<<<2 * p.workers, tc::kThreads, tc_smem_bytes(), stream>>>(a, b, o, w, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t stream) {
   static_assert(sizeof(tc::Smem) + 1024 <= 227 * 1024, "shared memory budget");
-  CUtensorMap tm_lat, tm_rope;
+  CUtensorMap tm_lat, tm_rope, tm_out, tm_part;
   memset(&tm_lat, 0, sizeof(tm_lat));
   memset(&tm_rope, 0, sizeof(tm_rope));
+  // outputs: [B*q_len*H, 512] bf16 and the partials [slots*H, 512] fp32, 16 x 16 boxes
+  const int units = p.B * p.q_len;
+  if (!encode_rows_map(&tm_out, p.out, (size_t)units * p.H, 2, CU_TENSOR_MAP_SWIZZLE_32B)) return cudaErrorInvalidValue;
+  if (p.slots_cap > 0) {
+    if (!encode_rows_map(&tm_part, p.ws + partial_o_offset(), (size_t)p.slots_cap * p.H, 4, CU_TENSOR_MAP_SWIZZLE_64B))
+      return cudaErrorInvalidValue;
+  } else {
+    tm_part = tm_out;  // never stored through: no item has a partial slot
+  }
   if (p.kv_dtype == MLA_KV_BF16) {
     if (!encode_cache_map(&tm_lat, p.cache, p.num_pages, p.page_size, 64, 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_cache_map(&tm_rope, p.cache, p.num_pages, p.page_size, 32, 2, CU_TENSOR_MAP_SWIZZLE_64B))
       return cudaErrorInvalidValue;
-    return launch_tc<MLA_KV_BF16>(tm_lat, tm_rope, p, stream);
+    return launch_tc<MLA_KV_BF16>(tm_lat, tm_rope, tm_out, tm_part, p, stream);
   }
   if (p.kv_dtype == MLA_KV_FP8_E4M3) {
     if (!encode_cache_map(&tm_lat, p.cache, p.num_pages, p.page_size, 256, 1, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_cache_map(&tm_rope, p.cache, p.num_pages, p.page_size, 32, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
-    return launch_tc<MLA_KV_FP8_E4M3>(tm_lat, tm_rope, p, stream);
+    return launch_tc<MLA_KV_FP8_E4M3>(tm_lat, tm_rope, tm_out, tm_part, p, stream);
   }
-  return launch_tc<MLA_KV_NVFP4>(tm_lat, tm_rope, p, stream);
+  return launch_tc<MLA_KV_NVFP4>(tm_lat, tm_rope, tm_out, tm_part, p, stream);
 }
 
 }  // namespace mla
