@@ -17,7 +17,7 @@
 namespace mla {
 cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t stream);
 int tc_max_clusters();
-cudaError_t launch_splitk_reduce(const uint8_t* ws, int U, int H, int slots_cap, uint16_t* out,
+cudaError_t launch_splitk_reduce(uint8_t* ws, int U, int H, int slots_cap, int status_ctas, uint16_t* out,
                                  float* lse, cudaStream_t stream, bool pdl);
 }  // namespace mla
 
@@ -42,6 +42,7 @@ cudaError_t current_workers(int* workers) {
     int w = sms >= 2 ? sms / 2 : 1;
     int clusters = mla::tc_max_clusters();
     if (clusters > 0 && clusters < w) w = clusters;
+    if (w > mla::kMaxCtas / 2) w = mla::kMaxCtas / 2;  // one status word per CTA in the header
     g_workers[dev] = w;
   }
   *workers = g_workers[dev];
@@ -183,10 +184,11 @@ MLA_EXPORT mla_status_t mla_decode(const void* q_nope, const void* q_pe, const v
   p.lse = lse;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(workspace, 0, 16, s) != cudaSuccess) return MLA_ERR_CUDA;
+  // No host-side reset: each decode CTA writes its status word at exit and the reduce (which
+  // always runs, after the decode) folds them into the call's status word.
   cudaError_t le = mla::launch_decode_tc(p, s);
   if (le != cudaSuccess) return MLA_ERR_CUDA;
-  if (mla::launch_splitk_reduce(p.ws, U, H, p.slots_cap, p.out, lse, s, true) != cudaSuccess)
+  if (mla::launch_splitk_reduce(p.ws, U, H, p.slots_cap, 2 * p.workers, p.out, lse, s, true) != cudaSuccess)
     return MLA_ERR_CUDA;
   return MLA_OK;
 }
@@ -200,8 +202,8 @@ MLA_EXPORT mla_status_t mla_splitk_reduce(const void* workspace, size_t workspac
   if (!aligned(workspace, 256) || !aligned(out, 16) || (lse && !aligned(lse, 4))) return MLA_ERR_INVALID_ARG;
   if (workspace_bytes < mla::kHeaderBytes) return MLA_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (mla::launch_splitk_reduce(static_cast<const uint8_t*>(workspace), B * q_len, H,
-                                slots_that_fit(workspace_bytes, H), static_cast<uint16_t*>(out), lse, s,
+  if (mla::launch_splitk_reduce(static_cast<uint8_t*>(const_cast<void*>(workspace)), B * q_len, H,
+                                slots_that_fit(workspace_bytes, H), 0, static_cast<uint16_t*>(out), lse, s,
                                 false) != cudaSuccess)
     return MLA_ERR_CUDA;
   return MLA_OK;

@@ -27,14 +27,19 @@ constexpr int kMaxUnits = MLA_MAX_UNITS; // B * q_len
 constexpr int kNvfp4Group = 16;
 
 // Workspace layout (bytes):
-//   [0, 4)                      device status word (reset by the host each call)
+//   [0, 4)                      device status word (written by the split-K reduce each call)
 //   [4, 8)                      schedule mode written by the decode kernel
 //   [kPlanOffset, +8*units)     plan: per unit {parts, first partial slot}
+//   [kCtaStatusOffset, +4*CTAs) status bits of each decode CTA (written unconditionally at its
+//                               exit; the split-K reduce ORs them into the status word)
 //   [kHeaderBytes, ...)         partial outputs  fp32 [slots][H][512]
 //   then                        partial LSEs     fp32 [slots][H]
 constexpr size_t kPlanOffset = 256;
+constexpr size_t kCtaStatusOffset = 16384;
+constexpr int kMaxCtas = 2048;
 constexpr size_t kHeaderBytes = 32768;
-static_assert(kPlanOffset + 8 * (size_t)kMaxUnits <= kHeaderBytes, "plan must fit the header");
+static_assert(kPlanOffset + 8 * (size_t)kMaxUnits <= kCtaStatusOffset, "plan must fit below the CTA status words");
+static_assert(kCtaStatusOffset + 4 * (size_t)kMaxCtas <= kHeaderBytes, "CTA status words must fit the header");
 
 MLA_HD size_t partial_o_offset() { return kHeaderBytes; }
 MLA_HD size_t partial_lse_offset(int slots, int H) {

@@ -167,6 +167,7 @@ struct Smem {
   unsigned long long tmask[kStages];  // rows of the staged tile that are real, visible positions
   uint32_t tmem_base;
   int abort_flag;
+  unsigned status;  // this CTA's status bits
   int scratch[33];
   WorkerStart wstart;  // this worker's place in the schedule (the full plan is built in xbuf)
 };
@@ -285,7 +286,9 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
   {
     // the schedule is evaluated in the exchange buffers, which are idle until the first tile
     PlanSmem& plan = *reinterpret_cast<PlanSmem*>(&S.xbuf[0][0][0]);
-    compute_plan(p, plan, S.scratch, blockIdx.x == 0);
+    if (tid == 0) S.status = 0u;
+    __syncthreads();
+    compute_plan(p, plan, S.scratch, &S.status, blockIdx.x == 0);
     if (tid == 0) S.wstart = worker_start(p, plan, worker);
     __syncthreads();
   }
@@ -384,7 +387,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
           uint32_t bytes = 0;
           for (int j = 0; j < ti.npages; ++j) {
             if (ti.page_ok[j]) bytes += page_bytes;
-            else set_status(p.ws, MLA_STATUS_PAGE_OUT_OF_RANGE);
+            else set_status(&S.status, MLA_STATUS_PAGE_OUT_OF_RANGE);
           }
           S.tmask[st] = ti.rowmask;  // published by the arrive below
           ptx::mbar_arrive_expect_tx(b_kv_full + 8 * st, bytes);
@@ -678,7 +681,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
         }
         *reinterpret_cast<uint4*>(S.q_rope + row * 64 + ((c ^ ((row >> 1) & 3)) * 16)) = x;
       }
-      if (q_range) set_status(p.ws, MLA_STATUS_Q_RANGE);
+      if (q_range) set_status(&S.status, MLA_STATUS_Q_RANGE);
       ptx::fence_proxy_async_smem();
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
@@ -965,13 +968,13 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       }
     }
   }
-
   if (warp >= kWarpSoftmax0 && lane == 0) ptx::bulk_wait_all();  // epilogue stores done before exit
   // ------------------------------------------------------------------ teardown
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == kWarpMma) ptx::tmem_dealloc(tmem, kTmemCols);
-  if (tid == 0 && S.abort_flag) set_status(p.ws, MLA_STATUS_WAIT_TIMEOUT);
+  if (tid == 0 && blockIdx.x < kMaxCtas)
+    reinterpret_cast<unsigned*>(p.ws + kCtaStatusOffset)[blockIdx.x] = S.status | (S.abort_flag ? MLA_STATUS_WAIT_TIMEOUT : 0u);
   ptx::cluster_sync_all();
 }
 

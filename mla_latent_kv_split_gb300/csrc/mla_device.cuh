@@ -26,9 +26,8 @@ struct DecodeParams {
   float* lse;                 // [B, q_len, H] or nullptr
 };
 
-__device__ __forceinline__ void set_status(uint8_t* ws, unsigned bits) {
-  atomicOr(reinterpret_cast<unsigned*>(ws), bits);
-}
+// Status bits accumulate in a CTA-local word (shared memory) that the CTA stores at exit.
+__device__ __forceinline__ void set_status(unsigned* cta_status, unsigned bits) { atomicOr(cta_status, bits); }
 
 // Bytes per page of the cache.
 __host__ __device__ __forceinline__ size_t page_stride_bytes(int kv_dtype, int page_size) {
@@ -120,7 +119,7 @@ __device__ inline int block_exclusive_scan(int* vals, int n, int* scratch /*[33]
 // Evaluates the schedule in shared memory (all threads call).  Sets status bits for
 // malformed seq_lens.  When `write_plan` is set, also stores {parts, slot} per unit into
 // the workspace plan for the split-K reduce.
-__device__ inline void compute_plan(const DecodeParams& p, PlanSmem& pl, int* scratch,
+__device__ inline void compute_plan(const DecodeParams& p, PlanSmem& pl, int* scratch, unsigned* cta_status,
                                     bool write_plan) {
   const int T = blockDim.x * blockDim.y * blockDim.z;
   const int tid = threadIdx.x + blockDim.x * (threadIdx.y + blockDim.y * threadIdx.z);
@@ -139,7 +138,7 @@ __device__ inline void compute_plan(const DecodeParams& p, PlanSmem& pl, int* sc
     pl.begin[u] = p.num_splits > 0 ? (tiles ? cdiv_i(tiles, forced_span_tiles(vis, p.num_splits)) : 0)
                                    : tiles;
   }
-  if (bad && write_plan) set_status(p.ws, bad);
+  if (bad && write_plan) set_status(cta_status, bad);
   __syncthreads();
   int N = block_exclusive_scan(pl.begin, U, scratch);
   if (tid == 0) {

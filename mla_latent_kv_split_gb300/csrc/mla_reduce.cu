@@ -2,10 +2,16 @@
 // splitk_reduce on the per-split outputs and log-sum-exps).
 //
 // For a (b, i) cut into S > 1 parts with partials (o_s [H,512], lse_s [H]):
-//   M = max_s lse_s;  lse = M + log(sum_s exp(lse_s - M));  out = sum_s exp(lse_s - lse) o_s.
-// A (b, i) with nothing visible gets out = 0 and lse = -inf; one with a single part was
-// written by the decode kernel and is skipped.  One CTA of 128 threads per (unit, head):
-// each thread owns 4 consecutive output columns (one float4 per partial).
+//   lse = log sum_s exp(lse_s);  out = sum_s exp(lse_s - lse) o_s.
+// evaluated in one pass with a running maximum (parts taken two at a time).  A (b, i) with
+// nothing visible gets out = 0 and lse = -inf; one with a single part was written by the
+// decode kernel and is skipped.  After a decode, the first CTA also folds the decode CTAs'
+// status bits into the call's status word.
+//
+// One CTA of 256 threads per (unit, 8 heads): warp w takes one head, lane l its 16 output
+// columns [16 l, 16 l + 16), so a part's row of a head is one coalesced 2 KB read.  Every
+// load of a group of parts is issued before any is used: a part group costs one memory
+// round trip, and the whole grid (units x H / 8 CTAs) is resident at once.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -14,56 +20,86 @@
 
 namespace mla {
 
-constexpr int kReduceThreads = 128;
+constexpr int kReduceThreads = 256;
+constexpr int kReduceHeads = kReduceThreads / 32;
+constexpr int kPartGroup = 2;
 
-__global__ void __launch_bounds__(kReduceThreads)
-mla_splitk_reduce_kernel(const uint8_t* __restrict__ ws, int U, int H, int slots_cap,
+__global__ void __launch_bounds__(kReduceThreads, 4)
+mla_splitk_reduce_kernel(uint8_t* __restrict__ ws, int U, int H, int slots_cap, int status_ctas,
                          uint16_t* __restrict__ out, float* __restrict__ lse) {
   // Programmatic dependent launch: everything before this point overlaps the decode
   // kernel's tail; the plan and partials are read only after the decode has completed.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int u = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  if (status_ctas > 0 && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < 32) {
+    // the call's status word: the OR of every decode CTA's status bits
+    unsigned bits = 0;
+    for (int c = threadIdx.x; c < status_ctas; c += 32) bits |= reinterpret_cast<const unsigned*>(ws + kCtaStatusOffset)[c];
+    bits = __reduce_or_sync(0xffffffffu, bits);
+    if (threadIdx.x == 0) *reinterpret_cast<unsigned*>(ws) = bits;
+  }
+  const int u = blockIdx.x, lane = threadIdx.x & 31;
+  const int h = blockIdx.y * kReduceHeads + (threadIdx.x >> 5);
+  if (h >= H) return;
   const int2 pl = reinterpret_cast<const int2*>(ws + kPlanOffset)[u];
   const int parts = pl.x, slot = pl.y;
-  const size_t row = (size_t)u * H + h;
   if (parts == 1) return;
-  uint2 packed;
-  float lse_v;
-  if (parts <= 0 || slot < 0 || slot + parts > slots_cap) {
-    packed = make_uint2(0u, 0u);
-    lse_v = -INFINITY;
-  } else {
+  const size_t row = (size_t)u * H + h;
+  float acc[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+  float m = -INFINITY, l = 0.f;
+  if (parts > 1 && slot >= 0 && slot + parts <= slots_cap) {
     const float* pls = reinterpret_cast<const float*>(ws + partial_lse_offset(slots_cap, H));
     const float4* po = reinterpret_cast<const float4*>(ws + partial_o_offset());
-    float M = -INFINITY;
-    for (int s = 0; s < parts; ++s) M = fmaxf(M, pls[(size_t)(slot + s) * H + h]);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (M == -INFINITY) {
-      lse_v = -INFINITY;
-    } else {
-      float tot = 0.f;
-      for (int s = 0; s < parts; ++s) tot += expf(pls[(size_t)(slot + s) * H + h] - M);
-      lse_v = M + logf(tot);
-      for (int s = 0; s < parts; ++s) {
-        float w = expf(pls[(size_t)(slot + s) * H + h] - lse_v);
-        float4 v = po[((size_t)(slot + s) * H + h) * (kLatent / 4) + tid];
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
+    for (int s0 = 0; s0 < parts; s0 += kPartGroup) {
+      float ls[kPartGroup];
+      float4 v[kPartGroup][4];
+#pragma unroll
+      for (int j = 0; j < kPartGroup; ++j) {
+        const bool ok = s0 + j < parts;
+        const size_t r = (size_t)(slot + s0 + j) * H + h;
+        ls[j] = ok ? pls[r] : -INFINITY;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[j][k] = ok ? po[r * (kLatent / 4) + 4 * lane + k] : make_float4(0.f, 0.f, 0.f, 0.f);
       }
+      float mn = m;
+#pragma unroll
+      for (int j = 0; j < kPartGroup; ++j) mn = fmaxf(mn, ls[j]);
+      if (mn == -INFINITY) continue;
+      const float sc = expf(m - mn);  // m = -inf -> 0
+      l *= sc;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) acc[k] *= sc;
+#pragma unroll
+      for (int j = 0; j < kPartGroup; ++j) {
+        const float w = expf(ls[j] - mn);  // missing parts: -inf -> 0
+        l += w;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          acc[4 * k] = fmaf(w, v[j][k].x, acc[4 * k]);
+          acc[4 * k + 1] = fmaf(w, v[j][k].y, acc[4 * k + 1]);
+          acc[4 * k + 2] = fmaf(w, v[j][k].z, acc[4 * k + 2]);
+          acc[4 * k + 3] = fmaf(w, v[j][k].w, acc[4 * k + 3]);
+        }
+      }
+      m = mn;
     }
-    packed.x = (unsigned)float_to_bf16_bits_rn(acc.x) | ((unsigned)float_to_bf16_bits_rn(acc.y) << 16);
-    packed.y = (unsigned)float_to_bf16_bits_rn(acc.z) | ((unsigned)float_to_bf16_bits_rn(acc.w) << 16);
   }
-  reinterpret_cast<uint2*>(out + row * kLatent)[tid] = packed;
-  if (lse && tid == 0) lse[row] = lse_v;
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  uint32_t pk[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    pk[k] = (uint32_t)float_to_bf16_bits_rn(acc[2 * k] * inv) | ((uint32_t)float_to_bf16_bits_rn(acc[2 * k + 1] * inv) << 16);
+  uint4* dst = reinterpret_cast<uint4*>(out + row * kLatent) + 2 * lane;
+  dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+  if (lse && lane == 0) lse[row] = l > 0.f ? m + logf(l) : -INFINITY;
 }
 
-cudaError_t launch_splitk_reduce(const uint8_t* ws, int U, int H, int slots_cap, uint16_t* out,
+cudaError_t launch_splitk_reduce(uint8_t* ws, int U, int H, int slots_cap, int status_ctas, uint16_t* out,
                                  float* lse, cudaStream_t stream, bool pdl) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(U, H);
+  cfg.gridDim = dim3(U, (H + kReduceHeads - 1) / kReduceHeads);
   cfg.blockDim = dim3(kReduceThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
@@ -72,7 +108,7 @@ cudaError_t launch_splitk_reduce(const uint8_t* ws, int U, int H, int slots_cap,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, mla_splitk_reduce_kernel, ws, U, H, slots_cap, out, lse);
+  return cudaLaunchKernelEx(&cfg, mla_splitk_reduce_kernel, ws, U, H, slots_cap, status_ctas, out, lse);
 }
 
 }  // namespace mla
