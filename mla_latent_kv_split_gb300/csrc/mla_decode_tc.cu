@@ -92,7 +92,8 @@ constexpr int kSoftmaxThreads = 256;
 // Registers per thread: the launch gives every thread kLaunchRegs; the control warpgroup
 // (warps 0..3) drops to ctrl, the sender warpgroup to sender, and the two softmax
 // warpgroups rise to softmax.  The sum must not exceed 512 * kLaunchRegs (65,536); the split
-// follows each cache format's register needs (the senders decode quantized tiles).
+// follows each cache format's register needs (FP8 tiles are decoded by the senders, NVFP4
+// tiles by the softmax warpgroups).
 constexpr uint32_t kLaunchRegs = 128;
 template <int KV>
 struct RegSplit;
@@ -106,7 +107,7 @@ struct RegSplit<MLA_KV_FP8_E4M3> {
 };
 template <>
 struct RegSplit<MLA_KV_NVFP4> {
-  static constexpr uint32_t ctrl = 72, sender = 136, softmax = 152;
+  static constexpr uint32_t ctrl = 64, sender = 96, softmax = 176;
 };
 template <int KV>
 constexpr bool reg_split_fits() {
@@ -131,9 +132,8 @@ struct TileInfo {
 
 struct Bars {
   uint64_t kv_full[kStages];   // TMA bytes landed
-  uint64_t kv_ready[kStages];  // tile prepared for the MMAs (quantized: decoded by the senders, every tile;
+  uint64_t kv_ready[kStages];  // tile prepared for the MMAs (quantized: decoded by a softmax warpgroup, every tile;
                                // bf16: masked rows zeroed by the producer warp, those tiles only)
-  uint64_t deq;                // senders read every raw byte of a tile (before decoding in place)
   uint64_t kv_empty[kStages];  // P.V of the tile completed: stage reusable
   uint64_t s_full[2];          // S MMAs of a buffer completed
   uint64_t s_free[2];          // the senders and the buffer's softmax warpgroup read its S
@@ -266,6 +266,76 @@ __device__ __forceinline__ int item_take(const int4* ring, uint32_t b_full, uint
   return v.z >= 0 ? 1 : 0;
 }
 
+// Quantized caches: decodes the raw FP8 / NVFP4 bytes of landed tile k in place into f16, in
+// the swizzled layouts the score and P.V MMAs read (rows that are not visible become zeros),
+// then releases the tile to the score MMAs.  Called by the 128 threads of one warpgroup
+// (tq = 0..127: row tq / 2, half-row tq & 1 = 18 chunks of 8 values); `bar_id` is that
+// warpgroup's named barrier, which separates every read of raw bytes from the in-place writes.
+template <int KV>
+__device__ __forceinline__ bool prepare_tile(Smem& S, const DecodeParams& p, int k, int tq, uint32_t cr,
+                                             uint32_t b_kv_full, uint32_t b_kv_ready, uint32_t bar_id,
+                                             volatile int* abort_flag) {
+  const int st = k % kStages;
+  if (!ptx::mbar_wait(b_kv_full + 8 * st, (k / kStages) & 1, abort_flag)) return false;
+  const int pr = tq >> 1, phf = tq & 1;
+  uint8_t* base = S.stage[st];
+  const bool valid = (S.tmask[st] >> pr) & 1ull;
+  uint32_t raw[18][2];
+  if (valid) {
+#pragma unroll
+    for (int i = 0; i < 18; ++i) {
+      const int c = 18 * phf + i;
+      if (KV == MLA_KV_FP8_E4M3) {
+        const uint2 v = *reinterpret_cast<const uint2*>(c < 32 ? base + kRawFp8 + pr * 256 + 8 * c
+                                                               : base + kRawFp8Rope + pr * 32 + 8 * (c - 32));
+        raw[i][0] = v.x;
+        raw[i][1] = v.y;
+      } else {
+        const int ps = p.page_size;
+        const int j = pr / ps, rin = pr - j * ps;
+        const uint8_t* page = base + kRawFp4 + j * ps * 324;
+        const int col0 = c < 32 ? 256 * (int)cr + 8 * c : 512 + 32 * (int)cr + 8 * (c - 32);
+        raw[i][0] = *reinterpret_cast<const uint32_t*>(page + rin * 288 + col0 / 2);
+        raw[i][1] = page[ps * 288 + rin * 36 + col0 / 16];
+      }
+    }
+  }
+  ptx::named_bar_sync(bar_id, 128);  // every raw byte of the tile is in registers
+#pragma unroll
+  for (int i = 0; i < 18; ++i) {
+    uint4 o = make_uint4(0u, 0u, 0u, 0u);
+    if (valid) {
+      if (KV == MLA_KV_FP8_E4M3) {
+        o.x = ptx::e4m3x2_to_f16x2((uint16_t)(raw[i][0] & 0xFFFFu));
+        o.y = ptx::e4m3x2_to_f16x2((uint16_t)(raw[i][0] >> 16));
+        o.z = ptx::e4m3x2_to_f16x2((uint16_t)(raw[i][1] & 0xFFFFu));
+        o.w = ptx::e4m3x2_to_f16x2((uint16_t)(raw[i][1] >> 16));
+      } else {
+        const uint32_t sc = ptx::e4m3x2_to_f16x2((uint16_t)(raw[i][1] | (raw[i][1] << 8)));
+        o.x = ptx::hmul2(ptx::e2m1x2_to_f16x2(raw[i][0] & 0xFFu), sc);
+        o.y = ptx::hmul2(ptx::e2m1x2_to_f16x2((raw[i][0] >> 8) & 0xFFu), sc);
+        o.z = ptx::hmul2(ptx::e2m1x2_to_f16x2((raw[i][0] >> 16) & 0xFFu), sc);
+        o.w = ptx::hmul2(ptx::e2m1x2_to_f16x2(raw[i][0] >> 24), sc);
+      }
+    }
+    // chunk c (8 values) of row pr: latent chunks in the 128-byte swizzle of their 64-column
+    // box, rope chunks in the 64-byte swizzle
+    const int c = 18 * phf + i;
+    *reinterpret_cast<uint4*>(c < 32 ? base + (c >> 3) * kLatBox + pr * 128 + (((c & 7) ^ (pr & 7)) * 16)
+                                     : base + 4 * kLatBox + pr * 64 + ((((c - 32) ^ ((pr >> 1) & 3))) * 16)) = o;
+  }
+  ptx::fence_proxy_async_smem();
+  ptx::mbar_arrive(b_kv_ready + 8 * st);
+  return true;
+}
+// Which warpgroup decodes a quantized cache: the senders (FP8: light decoding, done before
+// sending the previous tile's scores) or each softmax warpgroup for its own next tile (NVFP4:
+// heavier decoding, which would otherwise hold the senders back).
+template <int KV>
+constexpr bool decode_in_softmax() { return KV == MLA_KV_NVFP4; }
+template <int KV>
+constexpr bool decode_in_senders() { return KV == MLA_KV_FP8_E4M3; }
+
 // KV: cache format (MLA_KV_BF16 / MLA_KV_FP8_E4M3 / MLA_KV_NVFP4).  The MMAs run in bf16 for a
 // bf16 cache and in f16 for the quantized ones (E4M3 and E2M1 x E4M3 are exact in f16).
 template <int KV>
@@ -305,13 +375,12 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
   const uint32_t b_mma_final = ptx::smem_u32(&S.bars.mma_final);
   const uint32_t b_mma_final_pv = ptx::smem_u32(&S.bars.mma_final_pv);
   const uint32_t b_ep = ptx::smem_u32(&S.bars.ep);
-  const uint32_t b_deq = ptx::smem_u32(&S.bars.deq);
   const uint32_t b_item_full = ptx::smem_u32(&S.bars.item_full[0]), b_item_empty = ptx::smem_u32(&S.bars.item_empty[0]);
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(b_kv_full + 8 * s, 1);
-      ptx::mbar_init(b_kv_ready + 8 * s, KV == MLA_KV_BF16 ? 1 : kSenderThreads);
+      ptx::mbar_init(b_kv_ready + 8 * s, KV == MLA_KV_BF16 ? 1 : kWgThreads);
       ptx::mbar_init(b_kv_empty + 8 * s, 1);
     }
     for (int s = 0; s < 2; ++s) {
@@ -325,7 +394,6 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
     ptx::mbar_init(b_q_ready, kSenderThreads);
     ptx::mbar_init(b_o_free, kSoftmaxThreads);
     ptx::mbar_init(b_ep, kSoftmaxThreads);
-    ptx::mbar_init(b_deq, kSenderThreads);
     ptx::mbar_init(b_mma_final, 1);
     ptx::mbar_init(b_mma_final_pv, 1);
     for (int s = 0; s < kItemRing; ++s) {
@@ -538,70 +606,6 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
     const uint32_t t_s0 = tmem + lane_off + kTmemS, t_q = tmem + lane_off + kTmemQ;
     const uint32_t x_peer = ptx::mapa(ptx::smem_u32(&S.xbuf[0][0][0]), peer);
     const uint32_t bx_full_peer = ptx::mapa(b_x_full, peer);
-    const int tq = (warp - kWarpSender0) * 32 + lane;  // 0..127
-    const int pr = tq >> 1, phf = tq & 1;              // prepare: row and half-row (18 chunks of 8)
-
-    // (1) Quantized caches: tile k has landed; decode its FP8 / NVFP4 bytes in place to f16
-    // (masked rows become zeros).
-    auto prepare = [&](int k) -> bool {
-      const int st = k % kStages;
-      if (!ptx::mbar_wait(b_kv_full + 8 * st, (k / kStages) & 1, abort_flag)) return false;
-      uint8_t* base = S.stage[st];
-      const bool valid = (S.tmask[st] >> pr) & 1ull;
-      // destination of 16-byte chunk c (8 values) of row pr in the swizzled operand layout
-      auto chunk_ptr = [&](int c) -> uint4* {
-        return reinterpret_cast<uint4*>(c < 32 ? base + (c >> 3) * kLatBox + pr * 128 + (((c & 7) ^ (pr & 7)) * 16)
-                                              : base + 4 * kLatBox + pr * 64 + ((((c - 32) ^ ((pr >> 1) & 3))) * 16));
-      };
-      {
-        // every raw byte this thread needs -> registers, then (after all senders did the
-        // same) the decoded values over the same stage
-        uint32_t raw[18][2];
-        if (valid) {
-#pragma unroll
-          for (int i = 0; i < 18; ++i) {
-            const int c = 18 * phf + i;
-            if (KV == MLA_KV_FP8_E4M3) {
-              const uint2 v = *reinterpret_cast<const uint2*>(c < 32 ? base + kRawFp8 + pr * 256 + 8 * c
-                                                                     : base + kRawFp8Rope + pr * 32 + 8 * (c - 32));
-              raw[i][0] = v.x;
-              raw[i][1] = v.y;
-            } else {
-              const int ps = p.page_size;
-              const int j = pr / ps, rin = pr - j * ps;
-              const uint8_t* page = base + kRawFp4 + j * ps * 324;
-              const int col0 = c < 32 ? 256 * (int)cr + 8 * c : 512 + 32 * (int)cr + 8 * (c - 32);
-              raw[i][0] = *reinterpret_cast<const uint32_t*>(page + rin * 288 + col0 / 2);
-              raw[i][1] = page[ps * 288 + rin * 36 + col0 / 16];
-            }
-          }
-        }
-        ptx::mbar_arrive(b_deq);
-        if (!ptx::mbar_wait(b_deq, k & 1, abort_flag)) return false;
-#pragma unroll
-        for (int i = 0; i < 18; ++i) {
-          uint4 o = make_uint4(0u, 0u, 0u, 0u);
-          if (valid) {
-            if (KV == MLA_KV_FP8_E4M3) {
-              o.x = ptx::e4m3x2_to_f16x2((uint16_t)(raw[i][0] & 0xFFFFu));
-              o.y = ptx::e4m3x2_to_f16x2((uint16_t)(raw[i][0] >> 16));
-              o.z = ptx::e4m3x2_to_f16x2((uint16_t)(raw[i][1] & 0xFFFFu));
-              o.w = ptx::e4m3x2_to_f16x2((uint16_t)(raw[i][1] >> 16));
-            } else {
-              const uint32_t sc = ptx::e4m3x2_to_f16x2((uint16_t)(raw[i][1] | (raw[i][1] << 8)));
-              o.x = ptx::hmul2(ptx::e2m1x2_to_f16x2(raw[i][0] & 0xFFu), sc);
-              o.y = ptx::hmul2(ptx::e2m1x2_to_f16x2((raw[i][0] >> 8) & 0xFFu), sc);
-              o.z = ptx::hmul2(ptx::e2m1x2_to_f16x2((raw[i][0] >> 16) & 0xFFu), sc);
-              o.w = ptx::hmul2(ptx::e2m1x2_to_f16x2(raw[i][0] >> 24), sc);
-            }
-          }
-          *chunk_ptr(18 * phf + i) = o;
-        }
-      }
-      ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(b_kv_ready + 8 * st);
-      return true;
-    };
 
     // (2) Tile k's partial scores -> the peer CTA.
     auto send = [&](int k) -> bool {
@@ -687,12 +691,13 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       ptx::tc_fence_before();
       ptx::mbar_arrive(b_q_ready);
     };
-    // Per tile g: quantized caches decode tile g first (its S MMAs wait for it), then send
-    // tile g-1's scores.  An item's Q is loaded once the previous item's last scores have been
-    // read out of TMEM.
+    // Per tile g: when the senders decode (FP8), tile g is decoded first (its score MMAs wait
+    // for it), then tile g-1's scores are sent.  An item's Q is loaded once the previous
+    // item's last scores have been read out of TMEM.
     int g = 0;
     bool dead = false;
     WorkItem it;
+    const int tq = (warp - kWarpSender0) * 32 + lane;
     for (int k_item = 0; !dead; ++k_item) {
       const int got = item_take(S.items, b_item_full, b_item_empty, k_item, abort_flag, it, true);
       if (got <= 0) {
@@ -701,9 +706,18 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       }
       if (g == 0) load_q(it);  // the producer waits for it before its first cache load
       for (int t0 = it.tok_lo; t0 < it.tok_hi; t0 += kTileN, ++g) {
-        if (*abort_flag) { dead = true; break; }
-        if (KV != MLA_KV_BF16 && !prepare(g)) { dead = true; break; }
-        if (g > 0 && !send(g - 1)) { dead = true; break; }
+        if (*abort_flag) {
+          dead = true;
+          break;
+        }
+        if (decode_in_senders<KV>() && !prepare_tile<KV>(S, p, g, tq, cr, b_kv_full, b_kv_ready, 3, abort_flag)) {
+          dead = true;
+          break;
+        }
+        if (g > 0 && !send(g - 1)) {
+          dead = true;
+          break;
+        }
         if (t0 == it.tok_lo && g > 0) load_q(it);
       }
     }
@@ -751,6 +765,13 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       const int g0 = g;
       float m_own = -INFINITY, l_own = 0.f;  // this warpgroup's row sum and the reference it is relative to
       int t_idx = (g0 & 1) == wg ? 0 : 1;     // this warpgroup's first tile of the item
+      // quantized caches: this warpgroup decodes the tiles it will take (the first one now,
+      // each next one as soon as it has handed over the current one's P)
+      if (decode_in_softmax<KV>() && t_idx < nt &&
+          !prepare_tile<KV>(S, p, g0 + t_idx, 32 * q + lane, cr, b_kv_full, b_kv_ready, 4 + wg, abort_flag)) {
+        dead = true;
+        break;
+      }
       for (; t_idx < nt; t_idx += 2) {
         const int gg = g0 + t_idx;
         // ---- own partial scores
@@ -869,6 +890,12 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
         ptx::mbar_arrive(b_pf);
+        // quantized caches: decode this warpgroup's next tile of the item now
+        if (decode_in_softmax<KV>() && t_idx + 2 < nt &&
+            !prepare_tile<KV>(S, p, gg + 2, 32 * q + lane, cr, b_kv_full, b_kv_ready, 4 + wg, abort_flag)) {
+          dead = true;
+          break;
+        }
       }
       if (dead) break;
       g = g0 + nt;
