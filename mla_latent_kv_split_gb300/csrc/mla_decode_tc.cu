@@ -362,7 +362,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
     if (tid == 0) S.wstart = worker_start(p, plan, worker);
     __syncthreads();
   }
-  const WorkerStart wst = S.wstart;
+  const WorkerStart& wst = S.wstart;  // read from shared memory where needed
   const int n_tiles_total = wst.N;
 
   const uint32_t b_kv_full = ptx::smem_u32(&S.bars.kv_full[0]);
@@ -437,9 +437,6 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
         break;
       }
       const int b = it.u / p.q_len;
-      // Let the first item's queries reach the memory system before this CTA's burst of
-      // cache loads (otherwise they queue behind every SM's initial TMA traffic).
-      if (g == 0 && !ptx::mbar_wait(b_q_ready, 0, abort_flag)) break;
       TileInfo ti_next = tile_info(p, b, it.tok_lo, it.tok_hi);
       for (int t0 = it.tok_lo; t0 < it.tok_hi; t0 += kTileN, ++g) {
         // this tile's block-table entries were read one tile earlier, the next tile's are
@@ -698,13 +695,15 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
     bool dead = false;
     WorkItem it;
     const int tq = (warp - kWarpSender0) * 32 + lane;
+    // the first item's unit is known from the schedule: its Q loads overlap the item ring's
+    // start and the first cache loads
+    if (wst.busy) load_q(WorkItem{wst.u0, 0, 0, -1});
     for (int k_item = 0; !dead; ++k_item) {
       const int got = item_take(S.items, b_item_full, b_item_empty, k_item, abort_flag, it, true);
       if (got <= 0) {
         dead = got < 0;
         break;
       }
-      if (g == 0) load_q(it);  // the producer waits for it before its first cache load
       for (int t0 = it.tok_lo; t0 < it.tok_hi; t0 += kTileN, ++g) {
         if (*abort_flag) {
           dead = true;
@@ -765,18 +764,24 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       const int g0 = g;
       float m_own = -INFINITY, l_own = 0.f;  // this warpgroup's row sum and the reference it is relative to
       int t_idx = (g0 & 1) == wg ? 0 : 1;     // this warpgroup's first tile of the item
-      // quantized caches: this warpgroup decodes the tiles it will take (the first one now,
-      // each next one as soon as it has handed over the current one's P)
-      if (decode_in_softmax<KV>() && t_idx < nt &&
+      // The first item starts with one pass through the loop body that has no effect (every
+      // wait, arrive and store is skipped): it fetches the body's instructions while the
+      // first scores are still being computed, instead of on the first tile's critical path.
+      if (k_item == 0) t_idx -= 2;
+      // quantized caches: this warpgroup decodes the tiles it will take (each one as soon as
+      // it has handed over the previous one's P; on the first item, at the end of the
+      // instruction-fetch pass)
+      if (decode_in_softmax<KV>() && k_item > 0 && t_idx < nt &&
           !prepare_tile<KV>(S, p, g0 + t_idx, 32 * q + lane, cr, b_kv_full, b_kv_ready, 4 + wg, abort_flag)) {
         dead = true;
         break;
       }
       for (; t_idx < nt; t_idx += 2) {
+        const bool real = t_idx >= 0;
         const int gg = g0 + t_idx;
         // ---- own partial scores
         float s[64];
-        if (!ptx::mbar_wait(b_sf, (gg >> 1) & 1, abort_flag)) { dead = true; break; }
+        if (real && !ptx::mbar_wait(b_sf, (gg >> 1) & 1, abort_flag)) { dead = true; break; }
         ptx::tc_fence_after();
         {
           uint32_t r0[32], r1[32];
@@ -790,12 +795,12 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
           }
         }
         ptx::tc_fence_before();
-        ptx::mbar_arrive(b_sfree);
+        if (real) ptx::mbar_arrive(b_sfree);
         // ---- the peer's partial scores (pushed by its senders)
-        if (q == 0 && lane == 0) ptx::mbar_arrive_expect_tx(b_xf, kXBytes);
-        if (!ptx::mbar_wait(b_xf, (gg >> 1) & 1, abort_flag, true)) { dead = true; break; }
+        if (real && q == 0 && lane == 0) ptx::mbar_arrive_expect_tx(b_xf, kXBytes);
+        if (real && !ptx::mbar_wait(b_xf, (gg >> 1) & 1, abort_flag, true)) { dead = true; break; }
         // the peer pushed these only after P.V(gg-2) of this CTA had read the slot
-        if (gg - 2 > pv_known) pv_known = gg - 2;
+        if (real && gg - 2 > pv_known) pv_known = gg - 2;
         uint32_t xw[48];
 #pragma unroll
         for (int k = 0; k < kXGroups; ++k) {
@@ -819,8 +824,8 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
         // ---- mask (tail tiles only), row max (raw units; the scale is positive)
         // the producer published the tile's row mask with the tile's kv_full phase, which
         // completed before this tile's scores (and cannot move on before P(gg) is handed over)
-        const int st = gg % kStages;
-        if (!ptx::mbar_wait(b_kv_full + 8 * st, (gg / kStages) & 1, abort_flag)) { dead = true; break; }
+        const int st = real ? gg % kStages : 0;
+        if (real && !ptx::mbar_wait(b_kv_full + 8 * st, (gg / kStages) & 1, abort_flag)) { dead = true; break; }
         const uint64_t mask = S.tmask[st];
         if (mask != ~0ull) {
 #pragma unroll
@@ -844,10 +849,11 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
         }
         const bool grow = mt > m_prev + kRescaleThreshold;
         const float m_new = grow ? mt : m_prev;
-        *reinterpret_cast<volatile unsigned long long*>(chain) =
-            ((unsigned long long)(unsigned)(gg + 1) << 32) | __float_as_uint(m_new);
+        if (real)
+          *reinterpret_cast<volatile unsigned long long*>(chain) =
+              ((unsigned long long)(unsigned)(gg + 1) << 32) | __float_as_uint(m_new);
         // this warpgroup's running sum follows the reference
-        if (m_new != m_own) {
+        if (real && m_new != m_own) {
           if (l_own != 0.f) l_own *= ptx::ex2_approx(m_own - m_new);
           m_own = m_new;
         }
@@ -863,13 +869,15 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
           pk[c / 2] = KV == MLA_KV_BF16 ? __byte_perm(__float_as_uint(p0) + 0x8000u, __float_as_uint(p1) + 0x8000u, 0x7632)
                                         : ptx::pack_f16x2(p0, p1);
         }
-        l_own += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        if (real) l_own += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         // P(gg) -> the slot.  Row r, 16-byte chunk c (8 tokens) sits at chunk position
         // c ^ (r & 7) of the row's 128 bytes (the 128-byte swizzle the P.V MMAs read).
+        if (real) {
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(pslot + row * 128 + ((c ^ (row & 7)) * 16)) =
-              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(pslot + row * 128 + ((c ^ (row & 7)) * 16)) =
+                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        }
         if (t_idx > 0 && __any_sync(0xffffffffu, grow)) {
           // O (all 256 columns of these rows) moves to the new reference once P.V(gg-1) is
           // done, before P(gg) is handed over
@@ -889,7 +897,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
         }
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(b_pf);
+        if (real) ptx::mbar_arrive(b_pf);
         // quantized caches: decode this warpgroup's next tile of the item now
         if (decode_in_softmax<KV>() && t_idx + 2 < nt &&
             !prepare_tile<KV>(S, p, gg + 2, 32 * q + lane, cr, b_kv_full, b_kv_ready, 4 + wg, abort_flag)) {
@@ -923,16 +931,27 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       const CUtensorMap* tmap = direct ? &tm_out : &tm_part;
       const int row0 = (direct ? it.u : it.slot) * p.H + 32 * q;
       const bool store = direct || partial;
-      uint8_t* const stg = S.ostage[sw];
-      const uint32_t stg_a = ptx::smem_u32(stg);
+      // The worker's last item (the ring's next entry is the end marker): the cache stages
+      // are idle, so each chunk gets a staging buffer of its own there and all stores are in
+      // flight together.  Otherwise one 2 KB buffer per warp, reused chunk after chunk.
+      bool last = false;
+      {
+        const int s1 = (k_item + 1) % kItemRing;
+        if (ptx::mbar_test(b_item_full + 8 * s1, (uint32_t)((k_item + 1) / kItemRing) & 1u)) last = S.items[s1].z < 0;
+      }
+      last = __all_sync(0xffffffffu, last);
+      uint8_t* const stg0 = last ? S.stage[0] + sw * 16384 : S.ostage[sw];
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
         uint32_t r[16];
         ptx::tmem_ld16(t_o + 128 * wg + 16 * c, r);
         ptx::tmem_ld_wait();
-        // the previous chunk's stores (this item's or the last item's) have read the staging buffer
-        if (lane == 0) ptx::bulk_wait_read();
-        __syncwarp();
+        uint8_t* const stg = last ? stg0 + 2048 * c : stg0;
+        const uint32_t stg_a = ptx::smem_u32(stg);
+        if (!last) {  // the previous chunk's stores (this item's or the last item's) have read the buffer
+          if (lane == 0) ptx::bulk_wait_read();
+          __syncwarp();
+        }
         const int br = lane & 15;
         if (direct) {
           uint8_t* rowp = stg + (lane >> 4) * 512 + br * 32;
@@ -978,10 +997,19 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
     // item's query rows ahead of the senders' loads.
     regs_to<RegSplit<KV>::ctrl>();
     if (lane == 0) {
-      ItemCursor cur = item_cursor(p, wst, worker);
-      WorkItem nx;
+      // the first item comes from the schedule evaluated at start-up; the cursor (whose
+      // first step reproduces it) supplies the rest
+      ItemCursor cur{};
       for (int k = 0;; ++k) {
-        const bool more = next_item(p, n_tiles_total, cur, nx);
+        WorkItem nx = wst.first;
+        bool more = wst.busy != 0;
+        if (k > 0) {
+          if (k == 1) {  // the cursor starts at the first item, already published
+            cur = item_cursor(p, wst, worker);
+            next_item(p, n_tiles_total, cur, nx);
+          }
+          more = next_item(p, n_tiles_total, cur, nx);
+        }
         const int s = k % kItemRing;
         if (k >= kItemRing && !ptx::mbar_wait(b_item_empty + 8 * s, (uint32_t)((k / kItemRing) - 1) & 1u, abort_flag))
           break;

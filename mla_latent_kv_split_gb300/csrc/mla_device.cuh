@@ -237,20 +237,24 @@ __device__ inline void for_each_item(const DecodeParams& p, const PlanSmem& pl, 
 // Where worker c starts in the schedule: its first unit, that unit's first tile (heuristic
 // mode) or first item (forced mode), the partial slots used by earlier units, and the
 // total tile / item count.  From these the worker walks its items reading only seq_lens,
-// so the per-unit arrays of PlanSmem need not stay resident.
+// so the per-unit arrays of PlanSmem need not stay resident.  The worker's first item is
+// evaluated here as well, from the plan, so that it is known before any cursor runs.
 struct WorkerStart {
   int u0, base0, slot0, N;
+  int busy;        // the worker has at least one item
+  WorkItem first;  // its first item (when busy)
 };
 
 __device__ inline WorkerStart worker_start(const DecodeParams& p, const PlanSmem& pl, int c) {
   const int U = p.B * p.q_len;
-  WorkerStart w{0, 0, 0, pl.N};
+  WorkerStart w{0, 0, 0, pl.N, 0, WorkItem{0, 0, 0, -1}};
   if (pl.N <= 0) return w;
   int first;
+  int Ca = 0;
   if (p.num_splits > 0) {
     first = c;
   } else {
-    const int Ca = active_workers(pl.N, p.workers);
+    Ca = active_workers(pl.N, p.workers);
     if (c >= Ca) return w;
     first = (int)worker_begin(c, pl.N, Ca);
   }
@@ -259,6 +263,20 @@ __device__ inline WorkerStart worker_start(const DecodeParams& p, const PlanSmem
   w.u0 = u;
   w.base0 = pl.begin[u];
   w.slot0 = pl.pref[u];
+  w.busy = 1;
+  const int vis = pl.vis[u], tiles = cdiv_i(vis, kTile);
+  if (p.num_splits > 0) {  // item `first` is part k of unit u
+    const int k = first - w.base0;
+    const int span = forced_span_tiles(vis, p.num_splits);
+    const int lo = k * span, hi = min((k + 1) * span, tiles);
+    w.first = WorkItem{u, lo * kTile, min(hi * kTile, vis), pl.slot[u] >= 0 ? pl.slot[u] + k : -1};
+  } else {  // tiles [first, end of the worker's range or of the unit)
+    const long long e = worker_begin(c + 1, pl.N, Ca);
+    const int lo = first - w.base0;
+    const int hi = (int)(min(e, (long long)w.base0 + tiles) - w.base0);
+    w.first = WorkItem{u, lo * kTile, min(hi * kTile, vis),
+                       pl.slot[u] >= 0 ? pl.slot[u] + (c - worker_of(w.base0, pl.N, Ca)) : -1};
+  }
   return w;
 }
 
