@@ -424,6 +424,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
     // the whole warp waits for it to land and zeroes those rows, so that garbage, even NaN,
     // cannot reach P.V, then releases it to the score MMAs (kv_ready).
     const bool leader = lane == 0;
+    const uint64_t pol_stream = ptx::l2_policy_evict_first();  // cache rows are read once
     const uint32_t page_bytes = KV == MLA_KV_BF16 ? (uint32_t)p.page_size * (4 * 128 + 64)
                               : KV == MLA_KV_FP8_E4M3 ? (uint32_t)p.page_size * 288
                                                       : (uint32_t)p.page_size * 324;
@@ -464,15 +465,17 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
             if (KV == MLA_KV_BF16) {
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                ptx::tma_load_2d(dst + k * kLatBox + roff * 128, &tm_lat, 256 * (int)cr + 64 * k, y,
-                                 b_kv_full + 8 * st);
-              ptx::tma_load_2d(dst + 4 * kLatBox + roff * 64, &tm_rope, 512 + 32 * (int)cr, y, b_kv_full + 8 * st);
+                ptx::tma_load_2d_hint(dst + k * kLatBox + roff * 128, &tm_lat, 256 * (int)cr + 64 * k, y,
+                                      b_kv_full + 8 * st, pol_stream);
+              ptx::tma_load_2d_hint(dst + 4 * kLatBox + roff * 64, &tm_rope, 512 + 32 * (int)cr, y, b_kv_full + 8 * st,
+                                    pol_stream);
             } else if (KV == MLA_KV_FP8_E4M3) {
-              ptx::tma_load_2d(dst + kRawFp8 + roff * 256, &tm_lat, 256 * (int)cr, y, b_kv_full + 8 * st);
-              ptx::tma_load_2d(dst + kRawFp8Rope + roff * 32, &tm_rope, 512 + 32 * (int)cr, y, b_kv_full + 8 * st);
+              ptx::tma_load_2d_hint(dst + kRawFp8 + roff * 256, &tm_lat, 256 * (int)cr, y, b_kv_full + 8 * st, pol_stream);
+              ptx::tma_load_2d_hint(dst + kRawFp8Rope + roff * 32, &tm_rope, 512 + 32 * (int)cr, y, b_kv_full + 8 * st,
+                                    pol_stream);
             } else {
-              ptx::bulk_load(dst + kRawFp4 + j * page_bytes, p.cache + (size_t)ti.page[j] * page_bytes, page_bytes,
-                             b_kv_full + 8 * st);
+              ptx::bulk_load_hint(dst + kRawFp4 + j * page_bytes, p.cache + (size_t)ti.page[j] * page_bytes, page_bytes,
+                                  b_kv_full + 8 * st, pol_stream);
             }
           }
         }
@@ -976,7 +979,10 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
           const int x = 256 * (int)cr + 128 * wg + 16 * c;
 #pragma unroll
           for (int h = 0; h < 2; ++h)
-            if (32 * q + 16 * h < p.H) ptx::tma_store_2d(tmap, stg_a + h * (direct ? 512 : 1024), x, row0 + 16 * h);
+            if (32 * q + 16 * h < p.H) {
+              if (direct) ptx::tma_store_2d(tmap, stg_a + h * 512, x, row0 + 16 * h);
+              else ptx::tma_store_2d_hint(tmap, stg_a + h * 1024, x, row0 + 16 * h, ptx::l2_policy_evict_last());
+            }
           ptx::bulk_commit();
         }
       }
