@@ -185,6 +185,19 @@ def make_inputs(w: Workload, chunk_pages: int = 1024) -> dict:
                 workload=w)
 
 
+def draw_sinks(H: int, seed: int = 0, lo: float = 0.0, hi: float = 12.0) -> np.ndarray:
+    """Per-head sink logits ``[H]`` float32 for the attention-sink cases: uniform in
+    ``[lo, hi]`` (the range of a decode's log-sum-exp over a few to tens of thousands of
+    positions at these query/key scales), with every 8th head at -inf (a head without a
+    sink) and head 1 at ``hi + 20`` (a sink that takes nearly all of the weight)."""
+    g = torch.Generator().manual_seed(1000 + seed)
+    s = (lo + (hi - lo) * torch.rand((H,), generator=g)).numpy().astype(np.float32)
+    s[::8] = -np.inf
+    if H > 1:
+        s[1] = np.float32(hi + 20.0)
+    return s
+
+
 def poison_unused(inp: dict, rng_seed: int = 1) -> None:
     """Overwrite every cache position a request never reads (tails of its last page and
     whole unused pages) with NaN / garbage bytes, in place."""

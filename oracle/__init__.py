@@ -16,6 +16,7 @@ from .mla_ref import (  # noqa: F401
     dequant_pages,
     gather_tokens,
     visible_len,
+    window_range,
     mla_decode_ref,
     mla_decode_one,
     mla_partial_ref,

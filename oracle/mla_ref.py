@@ -32,6 +32,12 @@ Readings where the pages are silent (each also listed in the design notes):
 * NVFP4 page: token-major data, 288 bytes per token, element ``2j`` in the LOW nibble of
   byte ``j`` and ``2j+1`` in the high nibble; then token-major scales, 36 per token, scale
   ``g`` covering elements ``16g .. 16g+15`` (rope included); no second-level scale.
+* Sliding window and attention sinks (metrale ``mla_paged_decode_fp8`` takes
+  ``sliding_window`` and nullable per-head fp32 ``sinks`` without defining them): with a
+  window ``W > 0`` query ``i`` sees only the last ``W`` of its visible positions,
+  ``[max(0, V - W), V)``; a sink is one extra logit per head, in the units of the scaled
+  scores ``x``, that enters the softmax normalisation and carries no value:
+  ``lse = log(sum_t exp(x_t) + exp(sink))``, ``out = sum_t exp(x_t - lse) v_t``.
 """
 from __future__ import annotations
 
@@ -159,30 +165,45 @@ def _query_rows(q_nope_bits: np.ndarray, q_pe_bits: np.ndarray) -> np.ndarray:
     return np.concatenate([decode_bf16(q_nope_bits), decode_bf16(q_pe_bits)], axis=-1)
 
 
-def mla_decode_one(q: np.ndarray, keys: np.ndarray, sm_scale: float):
+def mla_decode_one(q: np.ndarray, keys: np.ndarray, sm_scale: float, sink=None):
     """Softmax attention of ``q [H, 576]`` over ``keys [n, 576]`` with ``V = keys[:, :512]``.
 
-    ``x[h, t] = sm_scale * q[h] . keys[t]``;  ``lse[h] = log sum_t exp(x[h, t])``;
-    ``out[h] = sum_t exp(x[h, t] - lse[h]) * keys[t, :512]``.  With ``n = 0``: out 0, lse -inf.
+    ``x[h, t] = sm_scale * q[h] . keys[t]``;  ``lse[h] = log(sum_t exp(x[h, t]) [+ exp(sink[h])])``;
+    ``out[h] = sum_t exp(x[h, t] - lse[h]) * keys[t, :512]``.  ``sink [H]`` (optional) is an
+    extra logit per head with no value.  With ``n = 0`` and no sink: out 0, lse -inf.
     """
     H = q.shape[0]
     n = keys.shape[0]
-    if n == 0:
+    x = np.float64(sm_scale) * (q @ keys.T) if n else np.zeros((H, 0))  # [H, n]
+    logits = x if sink is None else np.concatenate([x, np.asarray(sink, np.float64)[:, None]], axis=1)
+    if logits.shape[1] == 0:
         return np.zeros((H, LATENT_DIM)), np.full((H,), -np.inf)
-    x = np.float64(sm_scale) * (q @ keys.T)  # [H, n]
-    m = x.max(axis=1, keepdims=True)
-    lse = m[:, 0] + np.log(np.exp(x - m).sum(axis=1))
-    p = np.exp(x - lse[:, None])
+    m = logits.max(axis=1)
+    empty = np.isneginf(m)  # every logit -inf (nothing visible and a -inf sink): sum is 0
+    ms = np.where(empty, 0.0, m)
+    z = np.exp(logits - ms[:, None]).sum(axis=1)
+    with np.errstate(divide="ignore"):
+        lse = np.where(empty, -np.inf, ms + np.log(np.where(empty, 1.0, z)))
+    p = np.exp(x - np.where(empty, 0.0, lse)[:, None])
+    p[empty] = 0.0
     return p @ keys[:, :LATENT_DIM], lse
+
+
+def window_range(n_visible: int, window: int):
+    """Positions a query with ``n_visible`` visible positions attends under a sliding window
+    of ``window`` (0: no window): ``[max(0, n_visible - window), n_visible)``."""
+    lo = n_visible - window if window > 0 and n_visible > window else 0
+    return lo, n_visible
 
 
 def mla_decode_ref(q_nope_bits, q_pe_bits, cache, block_table, seq_lens, sm_scale: float,
                    kv_dtype: str = "bf16", kv_scale: float = 1.0, page_size: int = 64,
-                   rows=None):
+                   rows=None, window: int = 0, sinks=None):
     """Reference decode.  ``q_nope_bits [B, q_len, H, 512]`` / ``q_pe_bits [B, q_len, H, 64]``
     are bf16 bit patterns (uint16); ``block_table [B, max_pages]`` / ``seq_lens [B]`` int.
     Returns float64 ``out [B, q_len, H, 512]`` and ``lse [B, q_len, H]``.  ``rows`` (optional)
-    restricts the work to a list of ``(b, i)`` pairs; the other entries stay NaN."""
+    restricts the work to a list of ``(b, i)`` pairs; the other entries stay NaN.
+    ``window`` / ``sinks [H]``: the sliding window and per-head sinks (see the header)."""
     B, q_len, H, _ = q_nope_bits.shape
     out = np.full((B, q_len, H, LATENT_DIM), np.nan)
     lse = np.full((B, q_len, H), np.nan)
@@ -192,9 +213,10 @@ def mla_decode_ref(q_nope_bits, q_pe_bits, cache, block_table, seq_lens, sm_scal
         L = int(seq_lens[b])
         if b not in cached:
             cached = {b: gather_tokens(cache, block_table[b], L, kv_dtype, page_size, kv_scale)}
-        keys = cached[b][: visible_len(L, q_len, i)]
+        lo, hi = window_range(visible_len(L, q_len, i), window)
+        keys = cached[b][lo:hi]
         q = _query_rows(q_nope_bits[b, i], q_pe_bits[b, i])
-        out[b, i], lse[b, i] = mla_decode_one(q, keys, sm_scale)
+        out[b, i], lse[b, i] = mla_decode_one(q, keys, sm_scale, sink=sinks)
     return out, lse
 
 

@@ -303,3 +303,144 @@ def test_forced_split_ranges():
     assert oracle.forced_split_ranges(300, 2) == [(0, 192), (192, 300)]
     assert oracle.forced_split_ranges(10, 4) == [(0, 10)]
     assert oracle.forced_split_ranges(0, 3) == [(0, 0)]
+
+
+# ---------------------------------------------------------------------- sliding window and sinks
+
+def _windowed(inp, w, window, sinks=None):
+    return oracle.mla_decode_ref(inp["q_nope"], inp["q_pe"], inp["cache"], inp["block_table"], inp["seq_lens"],
+                                 w.sm_scale, kv_dtype=w.kv_dtype, kv_scale=inp["kv_scale"], page_size=w.page_size,
+                                 window=window, sinks=sinks)
+
+
+def test_window_range_cases():
+    assert oracle.window_range(10, 0) == (0, 10)
+    assert oracle.window_range(10, 3) == (7, 10)
+    assert oracle.window_range(10, 10) == (0, 10)
+    assert oracle.window_range(10, 11) == (0, 10)
+    assert oracle.window_range(0, 4) == (0, 0)
+    assert oracle.window_range(1, 1) == (0, 1)
+
+
+def test_window_at_least_visible_length_is_no_window():
+    w = W.WORKLOADS["paged_bf16_ragged"].scaled(B=3, H=4, q_len=2, seq_lens_override=(5, 130, 64))
+    inp = W.make_inputs(w)
+    o0, l0 = _windowed(inp, w, 0)
+    o1, l1 = _windowed(inp, w, 130)
+    assert np.array_equal(o0, o1) and np.array_equal(l0, l1)
+
+
+def test_window_one_returns_the_last_visible_row():
+    w = W.WORKLOADS["paged_bf16_ragged"].scaled(B=2, H=3, q_len=2, seq_lens_override=(77, 2))
+    inp = W.make_inputs(w)
+    out, lse = _windowed(inp, w, 1)
+    for b in range(2):
+        L = int(inp["seq_lens"][b])
+        keys = oracle.gather_tokens(inp["cache"], inp["block_table"][b], L, "bf16", 64)
+        for i in range(2):
+            t = L - 2 + i  # the newest position query i sees
+            assert np.array_equal(out[b, i], np.broadcast_to(keys[t, :512], (3, 512)))
+            q = np.concatenate([oracle.decode_bf16(inp["q_nope"][b, i]), oracle.decode_bf16(inp["q_pe"][b, i])], -1)
+            assert np.max(np.abs(lse[b, i] - w.sm_scale * (q @ keys[t]))) < 1e-12
+
+
+@pytest.mark.parametrize("window", [1, 40, 64, 65, 100])
+def test_window_equals_sdpa_with_a_band_mask(window):
+    q_len = 3
+    w = W.WORKLOADS["paged_fp8"].scaled(B=2, H=4, q_len=q_len, page_size=32, seq_lens_override=(150, 70))
+    inp = W.make_inputs(w)
+    out, lse = _windowed(inp, w, window)
+    for b in range(2):
+        L = int(inp["seq_lens"][b])
+        keys = torch.from_numpy(oracle.gather_tokens(inp["cache"], inp["block_table"][b], L, "fp8", 32,
+                                                     inp["kv_scale"]))
+        q = torch.from_numpy(np.concatenate([oracle.decode_bf16(inp["q_nope"][b]),
+                                             oracle.decode_bf16(inp["q_pe"][b])], -1))  # [q_len, H, 576]
+        t = torch.arange(L)[None, :]
+        newest = (L - q_len + torch.arange(q_len))[:, None]  # last position query i sees
+        mask = (t <= newest) & (t > newest - window)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            q.permute(1, 0, 2), keys[None].expand(4, L, 576), keys[None, :, :512].expand(4, L, 512),
+            attn_mask=mask[None].expand(4, q_len, L), scale=w.sm_scale).permute(1, 0, 2)
+        assert np.max(np.abs(ref.numpy() - out[b])) < 1e-12
+        x = w.sm_scale * torch.einsum("ihc,tc->iht", q, keys)
+        lref = torch.logsumexp(x.masked_fill(~mask[:, None, :], -math.inf), dim=-1)
+        assert np.max(np.abs(lref.numpy() - lse[b])) < 1e-12
+
+
+def test_window_equals_a_request_holding_only_the_window():
+    # the last W positions copied into a fresh request of length W give the same result
+    W_ = 70
+    w = W.WORKLOADS["paged_bf16_uniform"].scaled(B=1, H=4, page_size=64, seq_lens_override=(200,))
+    inp = W.make_inputs(w)
+    out, lse = _windowed(inp, w, W_)
+    keys_bits = np.concatenate([inp["cache"][p] for p in inp["block_table"][0, :4]])[:200]
+    short = np.zeros((2, 64, 576), dtype=np.uint16)
+    short.reshape(128, 576)[:W_] = keys_bits[200 - W_:]
+    o2, l2 = oracle.mla_decode_ref(inp["q_nope"], inp["q_pe"], short, np.array([[0, 1]], dtype=np.int32),
+                                   np.array([W_]), w.sm_scale)
+    assert np.array_equal(out, o2) and np.array_equal(lse, l2)
+
+
+def test_sink_minus_infinity_is_no_sink():
+    w = W.WORKLOADS["paged_bf16_ragged"].scaled(B=2, H=4, seq_lens_override=(90, 0))
+    inp = W.make_inputs(w)
+    o0, l0 = _windowed(inp, w, 0)
+    o1, l1 = _windowed(inp, w, 0, sinks=np.full(4, -np.inf))
+    # exp(-inf) adds an exact 0 to the normaliser; only the summation order may differ
+    assert np.array_equal(np.isneginf(l0), np.isneginf(l1)) and np.all(o1[1] == 0)
+    fin = np.isfinite(l0)
+    assert np.max(np.abs(o0 - o1)) < 1e-14 and np.max(np.abs(l0[fin] - l1[fin])) < 1e-13
+
+
+def test_sink_equal_to_the_single_score_halves_the_row():
+    qn, qp, cache = _contig_case(3, 1, seed=61)
+    q = np.concatenate([oracle.decode_bf16(qn[0, 0]), oracle.decode_bf16(qp[0, 0])], -1)
+    row = oracle.decode_bf16(cache[0, 0])
+    x = 0.05 * (q @ row)
+    out, lse = oracle.mla_decode_ref(qn, qp, cache, np.array([[0]]), np.array([1]), 0.05, page_size=1, sinks=x)
+    assert np.max(np.abs(out[0, 0] - 0.5 * row[None, :512])) < 1e-12
+    assert np.max(np.abs(lse[0, 0] - (x + math.log(2.0)))) < 1e-12
+
+
+def test_sink_with_nothing_visible():
+    w = W.WORKLOADS["paged_bf16_ragged"].scaled(B=1, H=3, q_len=2, seq_lens_override=(1,))
+    inp = W.make_inputs(w)
+    s = np.array([0.5, -2.0, -np.inf])
+    out, lse = _windowed(inp, w, 0, sinks=s)
+    assert np.all(out[0, 0] == 0) and np.array_equal(lse[0, 0], s)  # query 0 sees no position
+
+
+def test_sink_is_a_zero_value_token():
+    # A token whose latent part is 0 contributes nothing to the output; with its rope part
+    # solved so that each head's score equals that head's sink, attending it as an extra
+    # token must equal the sink.
+    H, n = 16, 29
+    rng = np.random.default_rng(71)
+    q = rng.standard_normal((H, 576))
+    keys = rng.standard_normal((n, 576))
+    scale = 0.09
+    sinks = rng.uniform(-1.0, 6.0, H)
+    k_pe = np.linalg.lstsq(q[:, 512:], sinks / scale, rcond=None)[0]
+    assert np.max(np.abs(scale * (q[:, 512:] @ k_pe) - sinks)) < 1e-12
+    extra = np.concatenate([np.zeros(512), k_pe])[None]
+    o_tok, l_tok = mla_ref.mla_decode_one(q, np.concatenate([keys, extra]), scale)
+    o_snk, l_snk = mla_ref.mla_decode_one(q, keys, scale, sink=sinks)
+    assert np.max(np.abs(o_tok - o_snk)) < 1e-11 and np.max(np.abs(l_tok - l_snk)) < 1e-11
+
+
+def test_window_and_sink_pure_python():
+    H, n, W_ = 2, 9, 4
+    qn, qp, cache = _contig_case(H, n, seed=81)
+    sinks = np.array([1.5, -0.25])
+    out, lse = oracle.mla_decode_ref(qn, qp, cache, np.array([[0]]), np.array([n]), 0.2, page_size=n,
+                                     window=W_, sinks=sinks)
+    qf = np.concatenate([oracle.decode_bf16(qn[0, 0]), oracle.decode_bf16(qp[0, 0])], -1).tolist()
+    kf = oracle.decode_bf16(cache[0]).tolist()
+    for h in range(H):
+        xs = [0.2 * math.fsum(qf[h][c] * kf[t][c] for c in range(576)) for t in range(n - W_, n)]
+        z = math.fsum([math.exp(x) for x in xs] + [math.exp(sinks[h])])
+        assert abs(lse[0, 0, h] - math.log(z)) < 1e-12
+        for c in range(0, 512, 41):
+            o = math.fsum(math.exp(x) / z * kf[n - W_ + j][c] for j, x in enumerate(xs))
+            assert abs(out[0, 0, h, c] - o) < 1e-12
