@@ -8,6 +8,13 @@ path against the measured HBM / bf16 peaks, an end-to-end figure through the C A
 host buffers, the float64 CPU oracle timed on a bounded sample, and the SM clocks seen.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+                    [--window W] [--sinks] [--op decode|kv_append|absorb] [--append-tokens T]
+
+``--window`` / ``--sinks`` time the sliding-window / attention-sink variant of the same
+call.  ``--op kv_append`` times the KV-cache append with quantise-on-write instead (the
+step before the decode): T new tokens (default B*q_len, one per query of the step) written
+into the workload's cache in its format; its own JSON line, HBM roofline.  ``--op absorb``
+times the Q absorption and V up-projection around the decode for the step's tokens.
 
 For N > 1 it is launched by torch.distributed.run, one rank per GPU; every rank decodes
 its own copy of the workload (independent replicas, weak scaling) and the slowest rank's
@@ -35,18 +42,28 @@ BYTES_PER_TOKEN = {"bf16": 1152, "fp8": 576, "nvfp4": 324}
 L2_FLUSH_BYTES = 512 << 20  # > 4x the 129 MB L2
 
 
-def algorithmic_work(inp) -> tuple[float, float, float]:
+def algorithmic_work(inp, window: int = 0) -> tuple[float, float, float]:
     """(bytes, flops, kv_bytes) one decode call must move / compute at minimum: the cache
-    rows of every visible position once, the queries, outputs, LSEs, the block-table
-    entries read and seq_lens; FLOPs of QK^T (576) and PV (512) per visible position."""
+    rows of every attended position once (the union of a request's query windows), the
+    queries, outputs, LSEs, the block-table entries read and seq_lens; FLOPs of QK^T (576)
+    and PV (512) per attended position and query."""
     import numpy as np
     w = inp["workload"]
     sl = np.clip(inp["seq_lens"].astype(np.int64), 0, None)
-    T = int(sl.sum())
+
+    def span(L, i):  # [lo, hi) attended by query i
+        hi = max(0, int(L) - w.q_len + i + 1)
+        return (hi - window if window > 0 and hi > window else 0), hi
+
+    T = sum(span(L, w.q_len - 1)[1] - span(L, 0)[0] if span(L, w.q_len - 1)[1] > 0 else 0 for L in sl)
     kv = T * BYTES_PER_TOKEN[w.kv_dtype]
     io = w.B * w.q_len * w.H * (576 * 2 + 512 * 2 + 4)
-    table = int(sum(-(-int(L) // w.page_size) for L in sl)) * 4 + 4 * w.B
-    vis = sum(max(0, int(L) - w.q_len + i + 1) for L in sl for i in range(w.q_len))
+    table = 0
+    for L in sl:
+        lo, hi = span(L, 0)[0], span(L, w.q_len - 1)[1]
+        table += (-(-hi // w.page_size) - lo // w.page_size) * 4 if hi > lo else 0
+    table += 4 * w.B
+    vis = sum(span(L, i)[1] - span(L, i)[0] for L in sl for i in range(w.q_len))
     flops = 2.0 * w.H * (576 + 512) * vis
     return float(kv + io + table), flops, float(kv)
 
@@ -132,7 +149,7 @@ class ClockSampler:
                     reasons=sorted(reasons), samples=len(sm))
 
 
-def cpu_oracle_sample(inp, seconds: float, start_b: int = 0):
+def cpu_oracle_sample(inp, seconds: float, start_b: int = 0, window: int = 0, sinks=None):
     """The float64 oracle, as it stands, on whole requests of the workload until `seconds`
     of CPU time have passed.  Returns (kv_bytes, elapsed, requests, rows)."""
     import oracle
@@ -144,8 +161,10 @@ def cpu_oracle_sample(inp, seconds: float, start_b: int = 0):
         bb = b % w.B
         oracle.mla_decode_ref(inp["q_nope"], inp["q_pe"], inp["cache"], inp["block_table"], inp["seq_lens"],
                               w.sm_scale, kv_dtype=w.kv_dtype, kv_scale=inp["kv_scale"], page_size=w.page_size,
-                              rows=[(bb, i) for i in range(w.q_len)])
-        kv_b += max(0, int(inp["seq_lens"][bb])) * BYTES_PER_TOKEN[w.kv_dtype]
+                              rows=[(bb, i) for i in range(w.q_len)], window=window,
+                              sinks=None if sinks is None else sinks.astype("float64"))
+        L = max(0, int(inp["seq_lens"][bb]))
+        kv_b += (min(L, window + w.q_len - 1) if window > 0 else L) * BYTES_PER_TOKEN[w.kv_dtype]
         n_req += 1
         rows += w.q_len
         b += 1
@@ -161,10 +180,14 @@ def cores_used() -> int:
         return os.cpu_count() or 1
 
 
-def workload_config(w, l2_note: str):
+def workload_config(w, l2_note: str, window: int = 0, sinks: bool = False):
     cfg = {"workload": w.name, "B": w.B, "q_len": w.q_len, "H": w.H, "page_size": w.page_size,
            "kv_dtype": w.kv_dtype, "sm_scale": "1/sqrt(192)", "num_splits": w.num_splits or "schedule",
            "l2": l2_note}
+    if window:
+        cfg["window"] = window
+    if sinks:
+        cfg["sinks"] = "per head, uniform in [0, 12], every 8th head -inf, head 1 at 32 (seeded)"
     if w.seq_len is not None:
         cfg["seq_len"] = w.seq_len
     if w.ragged is not None:
@@ -193,11 +216,15 @@ def run_reference(args):
     from mla_latent_kv_split_gb300 import workloads as W
     w = W.WORKLOADS[args.workload]
     inp = W.make_inputs(w)
+    if args.op != "decode":
+        print(json.dumps({"impl": "reference", "unavailable": "the oracle arm times the decode only"}), flush=True)
+        return
+    sinks = W.draw_sinks(w.H, seed=0) if args.sinks else None
     for s in range(args.warmup):
-        cpu_oracle_sample(inp, 0.0, start_b=s)
+        cpu_oracle_sample(inp, 0.0, start_b=s, window=args.window, sinks=sinks)
     t_steps, kv_total, rows_total = [], 0.0, 0
     for s in range(args.steps):
-        kv_b, el, n_req, rows = cpu_oracle_sample(inp, 0.0, start_b=args.warmup + s)
+        kv_b, el, n_req, rows = cpu_oracle_sample(inp, 0.0, start_b=args.warmup + s, window=args.window, sinks=sinks)
         t_steps.append(el)
         kv_total += kv_b
         rows_total += rows
@@ -207,7 +234,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(w, "n/a (CPU)"),
+        "config": workload_config(w, "n/a (CPU)", args.window, args.sinks),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores_used(), "kind": "oracle",
                          "sample": f"one whole request (all {w.q_len} queries, {w.H} heads) per step, "
                                    f"{args.steps} steps, {rows_total} (b,i) rows"},
@@ -234,7 +261,12 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     w = W.WORKLOADS[args.workload]
     inp = W.make_inputs(w)
-    nbytes, flops, kv_bytes = algorithmic_work(inp)
+    if args.op == "kv_append":
+        return run_append(args, w, inp, world, rank, dev)
+    if args.op == "absorb":
+        return run_absorb(args, w, world, rank, dev)
+    nbytes, flops, kv_bytes = algorithmic_work(inp, args.window)
+    h_sinks = W.draw_sinks(w.H, seed=0) if args.sinks else None
 
     def to_dev(a, bf16=False):
         t = torch.from_numpy(a.view(np.int16) if bf16 else a)
@@ -248,6 +280,7 @@ def run_ours(args):
     ws = mb.alloc_workspace(w.B, w.q_len, w.H, w.num_splits, dev)
     out = torch.empty((w.B, w.q_len, w.H, 512), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.B, w.q_len, w.H), dtype=torch.float32, device=dev)
+    sinks = None if h_sinks is None else torch.from_numpy(h_sinks).to(dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_head = flush[: flush.numel() // 2]
 
@@ -263,7 +296,7 @@ def run_ours(args):
     def call():
         mb.mla_decode(q_nope, q_pe, cache, table, seq_lens, w.sm_scale, w.kv_dtype, inp["kv_scale"],
                       w.num_splits, page_size=w.page_size, num_pages=inp["num_pages"], workspace=ws, out=out,
-                      lse=lse, stream=stream)
+                      lse=lse, stream=stream, window=args.window, sinks=sinks)
 
     sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
     sampler.start()
@@ -317,7 +350,8 @@ def run_ours(args):
         d_sl.copy_(h_sl, non_blocking=True)
         mb.mla_decode(d_qn.view(torch.bfloat16), d_qp.view(torch.bfloat16), cache, d_bt, d_sl, w.sm_scale,
                       w.kv_dtype, inp["kv_scale"], w.num_splits, page_size=w.page_size,
-                      num_pages=inp["num_pages"], workspace=ws, out=out, lse=lse, stream=stream)
+                      num_pages=inp["num_pages"], workspace=ws, out=out, lse=lse, stream=stream,
+                      window=args.window, sinks=sinks)
         h_out.copy_(out.view(torch.int16), non_blocking=True)
         h_lse.copy_(lse, non_blocking=True)
         b.record(stream)
@@ -348,12 +382,13 @@ def run_ours(args):
     roof["roofline_us"] = 1e6 * max(t_mem, t_mma)
     roof["kernel"] = "mla_decode call (decode kernel + split-K combine)"
 
-    cpu_kv, cpu_el, cpu_req, cpu_rows = cpu_oracle_sample(inp, args.cpu_seconds)
+    cpu_kv, cpu_el, cpu_req, cpu_rows = cpu_oracle_sample(inp, args.cpu_seconds, window=args.window, sinks=h_sinks)
     line = {
         "metric": METRIC, "value": world * kv_bytes / t_s / 1e9, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_mean, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": workload_config(w, "flushed between steps (512 MB write, then 256 MB read so no dirty lines remain)"),
+        "config": workload_config(w, "flushed between steps (512 MB write, then 256 MB read so no dirty lines remain)",
+                                  args.window, args.sinks),
         "us_per_call": 1e3 * t_mean, "us_per_call_median": 1e3 * statistics.median(times_ms),
         "us_per_call_max": 1e3 * max(times_ms),
         "kv_gbs": kv_bytes / t_s / 1e9, "tflops": flops / t_s / 1e12,
@@ -374,6 +409,137 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_append(args, w, inp, world, rank, dev):
+    """The KV-cache append with quantise-on-write: T new tokens (bf16 [T, 576]) written to
+    distinct locations of the workload's cache, in its format.  Algorithmic bytes per token:
+    1152 read + the stored bytes (1152 / 576 / 324) + 8 for the location."""
+    import numpy as np
+    import torch
+    from mla_latent_kv_split_gb300 import binding as mb
+
+    T = args.append_tokens or w.B * w.q_len
+    cache_np = inp["cache"]
+    num_pages, ps = inp["num_pages"], w.page_size
+    if T > num_pages * ps:
+        raise SystemExit(f"--append-tokens {T} exceeds the cache's {num_pages * ps} locations")
+    g = torch.Generator().manual_seed(5)
+    x = (torch.randn((T, 576), generator=g) * 2).to(torch.bfloat16).to(dev)
+    slots = torch.randperm(num_pages * ps, generator=g)[:T].to(torch.int64).to(dev)
+    cache = torch.from_numpy(cache_np.view(np.int16) if cache_np.dtype == np.uint16 else cache_np).to(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_head = flush[: flush.numel() // 2]
+    stream = torch.cuda.current_stream(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def call():
+        mb.mla_kv_append(x[:, :512], x[:, 512:], slots, cache, page_size=ps, kv_dtype=w.kv_dtype,
+                         kv_scale=inp["kv_scale"], num_pages=num_pages, device_status=status, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        flush_head.sum()
+        call()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    sampler.start()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for s in range(args.steps):
+        flush.zero_()
+        flush_head.sum()
+        evs[s][0].record(stream)
+        call()
+        evs[s][1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    times_ms = [a.elapsed_time(b) for a, b in evs]
+    t_mean = sum(times_ms) / len(times_ms)
+    if rank != 0:
+        return
+    nbytes = T * (1152 + BYTES_PER_TOKEN[w.kv_dtype] + 8)
+    peaks = load_peaks()
+    achieved = nbytes / (t_mean * 1e-3) / 1e9
+    line = {
+        "metric": "KV-cache append with quantise-on-write, GB/s of algorithmic bytes", "value": world * achieved,
+        "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_mean,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.kv_dtype, "data": "synthetic",
+        "config": {"workload": w.name, "op": "kv_append", "tokens": T, "kv_dtype": w.kv_dtype, "page_size": ps,
+                   "l2": "flushed between steps"},
+        "us_per_call": 1e3 * t_mean, "us_per_call_max": 1e3 * max(times_ms),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm"], "traffic": None, "peak_source": peaks["source"],
+                     "kernel": "mla_kv_append_kernel"},
+        "device_status": int(status.item()), "clocks": clocks, "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_absorb(args, w, world, rank, dev):
+    """The two per-head projections around the decode for the step's T = B*q_len tokens:
+    Q absorption (q_nope [T, H, 128] read out of [T, H, 192] raw query rows, W_UK^T
+    [H, 512, 128]) and V up-projection (o_lat [T, H, 512], W_UV [H, 128, 512]).  One step =
+    both launches.  Algorithmic bytes: both weights once plus every activation read and
+    written once."""
+    import torch
+    from mla_latent_kv_split_gb300 import binding as mb
+
+    T, H = w.B * w.q_len, w.H
+    g = torch.Generator().manual_seed(3)
+    bf = lambda shape, sc=1.0: (torch.randn(shape, generator=g) * sc).to(torch.bfloat16).to(dev)
+    q_raw = bf((T, H, 192))
+    w_ukT = bf((H, 512, 128), 128 ** -0.5)
+    o_lat = bf((T, H, 512), 0.2)
+    w_uv = bf((H, 128, 512), 512 ** -0.5)
+    q_lat = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+    o = torch.empty((T, H, 128), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_head = flush[: flush.numel() // 2]
+    stream = torch.cuda.current_stream(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def call():
+        mb.mla_batched_gemv(q_raw[:, :, :128], w_ukT, out=q_lat, device_status=status, stream=stream)
+        mb.mla_batched_gemv(o_lat, w_uv, out=o, device_status=status, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        flush_head.sum()
+        call()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    sampler.start()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for s in range(args.steps):
+        flush.zero_()
+        flush_head.sum()
+        evs[s][0].record(stream)
+        call()
+        evs[s][1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    times_ms = [a.elapsed_time(b) for a, b in evs]
+    t_mean = sum(times_ms) / len(times_ms)
+    if rank != 0:
+        return
+    nbytes = 2 * H * 512 * 128 * 2 + 2 * T * H * (128 + 512) * 2
+    flops = 2 * 2.0 * T * H * 512 * 128
+    peaks = load_peaks()
+    achieved = nbytes / (t_mean * 1e-3) / 1e9
+    line = {
+        "metric": "MLA Q absorption + V up-projection (per-head batched GEMV), GB/s of algorithmic bytes",
+        "value": world * achieved, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t_mean, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "op": "absorb", "tokens": T, "H": H, "nope": 128, "latent": 512, "v": 128,
+                   "l2": "flushed between steps"},
+        "us_per_call": 1e3 * t_mean, "us_per_call_max": 1e3 * max(times_ms), "tflops": flops / (t_mean * 1e-3) / 1e12,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm"], "traffic": None, "peak_source": peaks["source"],
+                     "kernel": "mla_batched_gemv_kernel x2"},
+        "device_status": int(status.item()), "clocks": clocks, "gpu_launches": 2 * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -382,6 +548,10 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--window", type=int, default=0, help="sliding window (0: none)")
+    ap.add_argument("--sinks", action="store_true", help="per-head attention sinks")
+    ap.add_argument("--op", default="decode", choices=["decode", "kv_append", "absorb"])
+    ap.add_argument("--append-tokens", type=int, default=0, help="kv_append: tokens per call (default B*q_len)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

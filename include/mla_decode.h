@@ -17,6 +17,9 @@
  *   - metrale "kv_cache_mla.rs", mla_paged_decode_nvfp4 / mla_paged_decode_fp8: 576
  *     values per token; an NVFP4 page is the packed E2M1 data section followed by one
  *     E4M3 scale per 16 values; FP8 pages hold one E4M3 byte per value and a scalar scale.
+ *     mla_paged_decode_fp8 also takes a sliding_window and nullable per-head fp32 sinks
+ *     (mla_decode_ex below; the page names the arguments without defining them, so the
+ *     reading used here is stated at mla_decode_ex).
  *
  * Conventions shared by every entry point:
  *   - All buffers belong to the caller.  The library never allocates or frees memory
@@ -70,6 +73,7 @@ typedef enum {
 #define MLA_STATUS_NEG_SEQ_LEN 0x8u       /* seq_len < 0 (treated as 0) */
 #define MLA_STATUS_WAIT_TIMEOUT 0x10u     /* a bounded in-kernel wait gave up */
 #define MLA_STATUS_Q_RANGE 0x20u          /* |q| beyond fp16 range on an FP8/NVFP4 cache */
+#define MLA_STATUS_SLOT_OUT_OF_RANGE 0x40u /* mla_kv_append: a location past the cache (skipped) */
 
 /* Limits of this build. */
 #define MLA_LATENT_DIM 512
@@ -117,8 +121,9 @@ mla_status_t mla_decode_workspace_size(int B, int q_len, int H, int num_splits, 
  *   out         [B, q_len, H, 512] bf16;  lse: [B, q_len, H] fp32 (may be NULL)
  *   stream      the CUDA stream everything is enqueued on.
  *
- * Enqueues: a reset of the status word, the decode kernel, and the split-K reduce.
- * Host-detected errors return before anything is enqueued.
+ * Enqueues two kernels: the decode, and the split-K reduce (which waits for the decode by
+ * programmatic dependent launch and also writes the status word).  No memset, no host
+ * synchronisation.  Host-detected errors return before anything is enqueued.
  */
 mla_status_t mla_decode(const void *q_nope, const void *q_pe, const void *kv_cache,
                         const int32_t *block_table, int max_pages, const int32_t *seq_lens,
@@ -127,17 +132,44 @@ mla_status_t mla_decode(const void *q_nope, const void *q_pe, const void *kv_cac
                         size_t workspace_bytes, void *out, float *lse, mla_stream_t stream);
 
 /*
+ * mla_decode with a sliding window and per-head attention sinks (metrale "kv_cache_mla.rs",
+ * mla_paged_decode_fp8, arguments sliding_window and sinks).  Every format is accepted.
+ *
+ *   window  0: no window.  W > 0: query i of request b attends only the last W of its
+ *           visible positions, t in [max(0, V - W), V) with V = seq_lens[b] - q_len + i + 1.
+ *   sinks   NULL: none.  Otherwise a device array [H] fp32: one extra logit per head, in
+ *           the units of the scaled scores (sm_scale and kv_scale already applied), that
+ *           joins the softmax normaliser but has no value row:
+ *             lse = log( sum_t exp(x_t) + exp(sinks[h]) ),  out = sum_t exp(x_t - lse) v_t.
+ *           -inf means "no sink" for that head; a (b, i) with nothing visible gets out 0
+ *           and lse = sinks[h].  Values are read on the device and not validated.
+ *
+ * num_splits > 0 cuts the window's tiles (64-token tiles from the one holding its first
+ * position) into at most num_splits ranges of cdiv(tiles, num_splits) tiles.  Errors and
+ * everything else as mla_decode; a negative window or a misaligned sinks pointer is
+ * MLA_ERR_INVALID_ARG.
+ */
+mla_status_t mla_decode_ex(const void *q_nope, const void *q_pe, const void *kv_cache,
+                           const int32_t *block_table, int max_pages, const int32_t *seq_lens,
+                           int B, int q_len, int H, int num_pages, int page_size, float sm_scale,
+                           int kv_dtype, float kv_scale, int num_splits, int window,
+                           const float *sinks, void *workspace, size_t workspace_bytes, void *out,
+                           float *lse, mla_stream_t stream);
+
+/*
  * The split-K combine on its own (TileGym splitk_reduce): for every (b, i) whose KV range
  * the last mla_decode on this workspace cut into several splits,
  *   lse = M + log sum_s exp(lse_s - M),  M = max_s lse_s,
  *   out = bf16( sum_s exp(lse_s - lse) * o_s );
  * all splits empty -> out 0, lse -inf.  (b, i) with nothing visible also get 0 / -inf;
- * unsplit (b, i) were written by the decode kernel and are left alone.
+ * unsplit (b, i) were written by the decode kernel and are left alone.  With `sinks`
+ * (device [H] fp32 or NULL, as in mla_decode_ex) the sink joins the combined normaliser,
+ * and (b, i) with nothing visible get lse = sinks[h]; pass the decode's own sinks.
  * mla_decode already enqueues this; it is exported for tests and for callers that run
  * the decode kernel and the combine on different schedules.  Same shapes as mla_decode.
  */
 mla_status_t mla_splitk_reduce(const void *workspace, size_t workspace_bytes, int B, int q_len,
-                               int H, void *out, float *lse, mla_stream_t stream);
+                               int H, const float *sinks, void *out, float *lse, mla_stream_t stream);
 
 /*
  * Copies the device status word of the last mla_decode on `workspace` to *device_status,
@@ -157,12 +189,73 @@ mla_status_t mla_decode_num_workers(int *workers);
  * Host copy of the device schedule, for tests: for the given seq_lens (HOST array), fills
  * per (b, i) unit: first tile, tile count, number of parts and first partial slot
  * (-1 when the unit is written directly); returns the number of partial slots used.
- * Arrays have B*q_len entries.  `workers` <= 0 means the current device's worker count.
+ * Arrays have B*q_len entries.  `window` as in mla_decode_ex (tile counts then start at
+ * the window's first tile).  `workers` <= 0 means the current device's worker count.
  */
 mla_status_t mla_decode_plan_host(const int32_t *seq_lens, int B, int q_len, int max_pages,
-                                  int page_size, int num_splits, int workers,
+                                  int page_size, int num_splits, int window, int workers,
                                   int32_t *unit_tile_begin, int32_t *unit_tiles,
                                   int32_t *unit_parts, int32_t *unit_slot, int32_t *slots_used);
+
+/*
+ * KV-cache append with quantise-on-write: stores this step's new tokens into the paged
+ * cache before a decode reads them (tokenspeed "tokenspeed_mla.py", forward_decode, which
+ * writes k[..., :512] and k[..., 512:] at out_cache_loc; metrale "kv_cache_mla.rs",
+ * mla_cache_assemble and the page layouts of the paged decode launchers).
+ *
+ *   latent      [T] rows of 512 bf16, row t at latent + t*latent_stride (elements)
+ *   rope        [T] rows of 64 bf16, row t at rope + t*rope_stride (elements); both pointers
+ *               16-byte aligned and both strides multiples of 8 (e.g. the two halves of
+ *               one [T, 576] tensor: rope = latent + 512, strides 576)
+ *   slots       [T] int64 device array: flat cache location page*page_size + row of token
+ *               t; negative = padding (skipped); >= num_pages*page_size is skipped and
+ *               sets MLA_STATUS_SLOT_OUT_OF_RANGE in *device_status.  Locations must be
+ *               distinct (two tokens for one location race).
+ *   kv_cache    the paged cache in kv_dtype's layout (mla_kv_dtype_t), num_pages pages,
+ *               page_size 32 or 64, 128-byte aligned
+ *   kv_dtype    bf16: values stored unchanged.  FP8: code = E4M3(x / kv_scale) (finite
+ *               kv_scale > 0).  NVFP4: per 16 values s = E4M3(amax / 6) and codes =
+ *               E2M1(x / value(s)), zero codes when value(s) is 0.  Quotients are fp32;
+ *               rounding is to nearest, ties to even, saturating (+-448 / +-6); a result
+ *               that rounds to zero keeps the sign of its input.  Inputs must be finite.
+ *   device_status  device uint32 that out-of-range locations OR a bit into (may be NULL;
+ *               never cleared by this call)
+ *
+ * Enqueues one kernel on `stream`; T == 0 enqueues nothing.  Host-detected errors (null or
+ * misaligned pointers, bad strides, sizes, format or scale) return before anything is
+ * enqueued.
+ */
+mla_status_t mla_kv_append(const void *latent, int64_t latent_stride, const void *rope,
+                           int64_t rope_stride, const int64_t *slots, int T, void *kv_cache,
+                           int num_pages, int page_size, int kv_dtype, float kv_scale,
+                           uint32_t *device_status, mla_stream_t stream);
+
+/*
+ * Per-head batched projection, one launch over all heads (metrale "kv_cache_mla.rs",
+ * mla_batched_gemv: output[head, n] = sum_k weight[head, n, k] * input[head, k], BF16),
+ * batched over T tokens:
+ *
+ *   out[t, h, n] = bf16( sum_k weight[h, n, k] * x[t, h, k] ),  fp32 accumulation.
+ *
+ * In absorbed MLA it is both steps around the decode: Q absorption (x = q_nope [T, H, 128],
+ * weight = W_UK^T per head [H, 512, 128], out = the decode's q_nope input [T, H, 512]) and
+ * V up-projection (x = the decode's out [T, H, 512], weight = W_UV [H, 128, 512]).
+ *
+ *   x       bf16, element (t, h, k) at x + t*x_token_stride + h*x_head_stride + k
+ *   weight  bf16 [H, N, K] contiguous
+ *   out     bf16, element (t, h, n) at out + t*out_token_stride + h*out_head_stride + n
+ *   Device pointers 16-byte aligned; x strides multiples of 8 with x_head_stride >= K and
+ *   x_token_stride >= H*x_head_stride; K a multiple of 8; T >= 0, H, N, K >= 1.
+ *   device_status: optional device uint32 that a bounded wait that gave up ORs
+ *   MLA_STATUS_WAIT_TIMEOUT into (never cleared by this call).
+ *
+ * Enqueues one kernel on `stream` (T == 0: nothing).  Host-detected errors return before
+ * anything is enqueued.
+ */
+mla_status_t mla_batched_gemv(const void *x, int64_t x_token_stride, int64_t x_head_stride,
+                              const void *weight, void *out, int64_t out_token_stride,
+                              int64_t out_head_stride, int T, int H, int N, int K,
+                              uint32_t *device_status, mla_stream_t stream);
 
 /*
  * mla_decode_no_alloc -- mla_decode for callers that cannot allocate device memory.

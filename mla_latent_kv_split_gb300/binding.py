@@ -20,12 +20,12 @@ MLA_KV_BF16, MLA_KV_FP8_E4M3, MLA_KV_NVFP4 = 0, 1, 2
 KV_DTYPE = {"bf16": MLA_KV_BF16, "fp8": MLA_KV_FP8_E4M3, "nvfp4": MLA_KV_NVFP4}
 STATUS_BITS = {
     0x1: "PAGE_OUT_OF_RANGE", 0x2: "SEQ_TOO_LONG", 0x4: "SEQ_LT_QLEN", 0x8: "NEG_SEQ_LEN",
-    0x10: "WAIT_TIMEOUT", 0x20: "Q_RANGE",
+    0x10: "WAIT_TIMEOUT", 0x20: "Q_RANGE", 0x40: "SLOT_OUT_OF_RANGE",
 }
 EXPORTED = (
     "mla_decode_abi_version", "mla_status_string", "mla_decode_workspace_size", "mla_decode",
     "mla_splitk_reduce", "mla_decode_read_status", "mla_decode_num_workers", "mla_decode_plan_host",
-    "mla_decode_no_alloc",
+    "mla_decode_no_alloc", "mla_decode_ex", "mla_kv_append", "mla_batched_gemv",
 )
 
 
@@ -56,15 +56,22 @@ def lib() -> ctypes.CDLL:
             h.mla_decode_workspace_size.argtypes = [I, I, I, I, ctypes.POINTER(Z)]
             h.mla_decode.restype = I
             h.mla_decode.argtypes = [P, P, P, P, I, P, I, I, I, I, I, F, I, F, I, P, Z, P, P, P]
+            h.mla_decode_ex.restype = I
+            h.mla_decode_ex.argtypes = [P, P, P, P, I, P, I, I, I, I, I, F, I, F, I, I, P, P, Z, P, P, P]
             h.mla_splitk_reduce.restype = I
-            h.mla_splitk_reduce.argtypes = [P, Z, I, I, I, P, P, P]
+            h.mla_splitk_reduce.argtypes = [P, Z, I, I, I, P, P, P, P]
             h.mla_decode_read_status.restype = I
             h.mla_decode_read_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
             h.mla_decode_num_workers.restype = I
             h.mla_decode_num_workers.argtypes = [ctypes.POINTER(I)]
             i32p = ctypes.POINTER(ctypes.c_int32)
             h.mla_decode_plan_host.restype = I
-            h.mla_decode_plan_host.argtypes = [i32p, I, I, I, I, I, I, i32p, i32p, i32p, i32p, i32p]
+            h.mla_decode_plan_host.argtypes = [i32p, I, I, I, I, I, I, I, i32p, i32p, i32p, i32p, i32p]
+            L64 = ctypes.c_int64
+            h.mla_kv_append.restype = I
+            h.mla_kv_append.argtypes = [P, L64, P, L64, P, I, P, I, I, I, F, P, P]
+            h.mla_batched_gemv.restype = I
+            h.mla_batched_gemv.argtypes = [P, L64, L64, P, P, L64, L64, I, I, I, I, P, P]
             h.mla_decode_no_alloc.restype = I
             h.mla_decode_no_alloc.argtypes = [P, P, P, P, I, P, I, I, I, I, I, F, I, F, I, P, P, P,
                                               ctypes.POINTER(P)]
@@ -115,11 +122,13 @@ def alloc_workspace(B: int, q_len: int, H: int, num_splits: int = 0, device=None
 
 def mla_decode(q_nope, q_pe, kv_cache, block_table, seq_lens, sm_scale: float, kv_dtype="bf16",
                kv_scale: float = 1.0, num_splits: int = 0, page_size: int | None = None,
-               num_pages: int | None = None, workspace=None, out=None, lse=None, stream=None):
-    """Calls ``mla_decode``.  Tensors: ``q_nope [B,q_len,H,512]`` / ``q_pe [B,q_len,H,64]``
-    bf16, ``kv_cache`` (``[P,ps,576]`` bf16 / uint8, or ``[P, ps*324]`` uint8 for NVFP4 with
-    ``page_size`` given), ``block_table [B,max_pages]`` int32, ``seq_lens [B]`` int32, all on
-    the device.  Returns ``(out, lse)`` (allocated with torch when not given)."""
+               num_pages: int | None = None, workspace=None, out=None, lse=None, stream=None,
+               window: int = 0, sinks=None):
+    """Calls ``mla_decode`` (or ``mla_decode_ex`` when ``window`` or ``sinks`` is given).
+    Tensors: ``q_nope [B,q_len,H,512]`` / ``q_pe [B,q_len,H,64]`` bf16, ``kv_cache``
+    (``[P,ps,576]`` bf16 / uint8, or ``[P, ps*324]`` uint8 for NVFP4 with ``page_size``
+    given), ``block_table [B,max_pages]`` int32, ``seq_lens [B]`` int32, ``sinks [H]`` fp32,
+    all on the device.  Returns ``(out, lse)`` (allocated with torch when not given)."""
     import torch
     B, q_len, H, _ = q_nope.shape
     kd = KV_DTYPE[kv_dtype] if isinstance(kv_dtype, str) else int(kv_dtype)
@@ -134,18 +143,21 @@ def mla_decode(q_nope, q_pe, kv_cache, block_table, seq_lens, sm_scale: float, k
     if lse is None:
         lse = torch.empty((B, q_len, H), dtype=torch.float32, device=q_nope.device)
     nbytes = workspace.numel() * workspace.element_size() if not isinstance(workspace, int) else 1 << 62
-    _check("mla_decode", lib().mla_decode(
-        _ptr(q_nope), _ptr(q_pe), _ptr(kv_cache), _ptr(block_table), int(block_table.shape[1]),
-        _ptr(seq_lens), B, q_len, H, int(num_pages), int(page_size), float(sm_scale), kd,
-        float(kv_scale), int(num_splits), _ptr(workspace), nbytes, _ptr(out), _ptr(lse),
-        _stream_ptr(stream)))
+    head = (_ptr(q_nope), _ptr(q_pe), _ptr(kv_cache), _ptr(block_table), int(block_table.shape[1]),
+            _ptr(seq_lens), B, q_len, H, int(num_pages), int(page_size), float(sm_scale), kd,
+            float(kv_scale), int(num_splits))
+    tail = (_ptr(workspace), nbytes, _ptr(out), _ptr(lse), _stream_ptr(stream))
+    if window or sinks is not None:
+        _check("mla_decode_ex", lib().mla_decode_ex(*head, int(window), _ptr(sinks), *tail))
+    else:
+        _check("mla_decode", lib().mla_decode(*head, *tail))
     return out, lse
 
 
-def mla_splitk_reduce(workspace, B: int, q_len: int, H: int, out, lse=None, stream=None):
+def mla_splitk_reduce(workspace, B: int, q_len: int, H: int, out, lse=None, stream=None, sinks=None):
     _check("mla_splitk_reduce", lib().mla_splitk_reduce(
-        _ptr(workspace), workspace.numel() * workspace.element_size(), B, q_len, H, _ptr(out), _ptr(lse),
-        _stream_ptr(stream)))
+        _ptr(workspace), workspace.numel() * workspace.element_size(), B, q_len, H, _ptr(sinks), _ptr(out),
+        _ptr(lse), _stream_ptr(stream)))
     return out, lse
 
 
@@ -159,7 +171,7 @@ def mla_decode_read_status(workspace, stream=None) -> int:
 
 
 def mla_decode_plan_host(seq_lens, q_len: int, max_pages: int, page_size: int, num_splits: int = 0,
-                         workers: int = 0):
+                         workers: int = 0, window: int = 0):
     """The schedule as the kernels evaluate it, computed on the host (for tests)."""
     sl = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
     B = sl.shape[0]
@@ -168,7 +180,7 @@ def mla_decode_plan_host(seq_lens, q_len: int, max_pages: int, page_size: int, n
     used = ctypes.c_int32(0)
     i32p = ctypes.POINTER(ctypes.c_int32)
     _check("mla_decode_plan_host", lib().mla_decode_plan_host(
-        sl.ctypes.data_as(i32p), B, q_len, max_pages, page_size, num_splits, workers,
+        sl.ctypes.data_as(i32p), B, q_len, max_pages, page_size, num_splits, int(window), workers,
         *[a.ctypes.data_as(i32p) for a in arrs], ctypes.byref(used)))
     return dict(tile_begin=arrs[0], tiles=arrs[1], parts=arrs[2], slot=arrs[3], slots_used=used.value)
 
@@ -196,3 +208,45 @@ def mla_decode_no_alloc(q_nope, q_pe, kv_cache, block_table, seq_lens, sm_scale:
         _ptr(seq_lens), B, q_len, H, int(num_pages), int(page_size), float(sm_scale), kd,
         float(kv_scale), int(num_splits), _ptr(out), _ptr(lse), _stream_ptr(stream), ctypes.byref(scratch)))
     return out, lse, scratch.value
+
+
+def mla_kv_append(latent, rope, slots, kv_cache, page_size: int | None = None, kv_dtype="bf16",
+                  kv_scale: float = 1.0, num_pages: int | None = None, device_status=None, stream=None):
+    """Calls ``mla_kv_append``: ``latent [T, 512]`` / ``rope [T, 64]`` bf16 row views (any
+    row stride that is a multiple of 8 elements, unit stride inside a row), ``slots [T]``
+    int64, all on the device; ``kv_cache`` as for :func:`mla_decode`; ``device_status`` an
+    optional int32/uint32 device tensor of one element that out-of-range slots OR a bit into."""
+    T = int(slots.shape[0])
+    kd = KV_DTYPE[kv_dtype] if isinstance(kv_dtype, str) else int(kv_dtype)
+    if page_size is None:
+        page_size = kv_cache.shape[1]
+    if num_pages is None:
+        num_pages = kv_cache.shape[0]
+    for t, w in ((latent, 512), (rope, 64)):
+        if T and (t.dim() != 2 or t.shape[0] != T or t.shape[1] != w or t.stride(1) != 1):
+            raise ValueError(f"expected a [{T}, {w}] row view with unit column stride, got {tuple(t.shape)}")
+    _check("mla_kv_append", lib().mla_kv_append(
+        _ptr(latent), int(latent.stride(0)) if T else 512, _ptr(rope), int(rope.stride(0)) if T else 64,
+        _ptr(slots), T, _ptr(kv_cache), int(num_pages), int(page_size), kd, float(kv_scale),
+        _ptr(device_status), _stream_ptr(stream)))
+    return kv_cache
+
+
+def mla_batched_gemv(x, weight, out=None, device_status=None, stream=None):
+    """Calls ``mla_batched_gemv``: ``x [T, H, K]`` bf16 (any token / head strides that are
+    multiples of 8 elements, unit stride along K), ``weight [H, N, K]`` bf16 contiguous,
+    ``out [T, H, N]`` bf16 (allocated with torch when not given; unit stride along N).
+    Returns ``out`` with ``out[t, h, n] = sum_k weight[h, n, k] * x[t, h, k]``."""
+    import torch
+    T, H, K = x.shape
+    H2, N, K2 = weight.shape
+    if (H2, K2) != (H, K) or x.stride(2) != 1 or not weight.is_contiguous():
+        raise ValueError(f"shapes x {tuple(x.shape)} / weight {tuple(weight.shape)} do not match")
+    if out is None:
+        out = torch.empty((T, H, N), dtype=torch.bfloat16, device=x.device)
+    if tuple(out.shape) != (T, H, N) or out.stride(2) != 1:
+        raise ValueError(f"out must be a [{T}, {H}, {N}] view with unit stride along N")
+    _check("mla_batched_gemv", lib().mla_batched_gemv(
+        _ptr(x), int(x.stride(0)), int(x.stride(1)), _ptr(weight), _ptr(out), int(out.stride(0)), int(out.stride(1)),
+        T, H, N, K, _ptr(device_status), _stream_ptr(stream)))
+    return out

@@ -17,8 +17,15 @@
 namespace mla {
 cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t stream);
 int tc_max_clusters();
-cudaError_t launch_splitk_reduce(uint8_t* ws, int U, int H, int slots_cap, int status_ctas, uint16_t* out,
-                                 float* lse, cudaStream_t stream, bool pdl);
+cudaError_t launch_splitk_reduce(uint8_t* ws, int U, int H, int slots_cap, int status_ctas, const float* sinks,
+                                 uint16_t* out, float* lse, cudaStream_t stream, bool pdl);
+cudaError_t launch_kv_append(const uint16_t* latent, long long latent_stride, const uint16_t* rope,
+                             long long rope_stride, const int64_t* slots, int T, uint8_t* cache, long long num_slots,
+                             int page_size, int kv_dtype, float kv_scale, uint32_t* status, cudaStream_t stream);
+cudaError_t launch_batched_gemv(const uint16_t* x, long long x_token_stride, long long x_head_stride,
+                                const uint16_t* w, uint16_t* out, long long out_token_stride,
+                                long long out_head_stride, int T, int H, int N, int K, uint32_t* status,
+                                cudaStream_t stream);
 }  // namespace mla
 
 namespace {
@@ -81,7 +88,7 @@ int slots_that_fit(size_t workspace_bytes, int H) {
 
 }  // namespace
 
-MLA_EXPORT int mla_decode_abi_version(void) { return 1; }
+MLA_EXPORT int mla_decode_abi_version(void) { return 2; }
 
 MLA_EXPORT const char* mla_status_string(mla_status_t s) {
   switch (s) {
@@ -112,13 +119,13 @@ MLA_EXPORT mla_status_t mla_decode_workspace_size(int B, int q_len, int H, int n
 }
 
 MLA_EXPORT mla_status_t mla_decode_plan_host(const int32_t* seq_lens, int B, int q_len, int max_pages,
-                                             int page_size, int num_splits, int workers,
+                                             int page_size, int num_splits, int window, int workers,
                                              int32_t* unit_tile_begin, int32_t* unit_tiles,
                                              int32_t* unit_parts, int32_t* unit_slot,
                                              int32_t* slots_used) {
   if (!seq_lens || !unit_tile_begin || !unit_tiles || !unit_parts || !unit_slot || !slots_used)
     return MLA_ERR_INVALID_ARG;
-  if (B < 1) return MLA_ERR_INVALID_ARG;
+  if (B < 1 || window < 0) return MLA_ERR_INVALID_ARG;
   mla_status_t st = check_shape(B, q_len, 16, num_splits);
   if (st != MLA_OK) return st;
   st = check_geometry(B, q_len, max_pages, 1, page_size);
@@ -126,7 +133,7 @@ MLA_EXPORT mla_status_t mla_decode_plan_host(const int32_t* seq_lens, int B, int
   int C = workers;
   if (C <= 0 && current_workers(&C) != cudaSuccess) return MLA_ERR_CUDA;
   std::vector<mla::UnitPlan> plan((size_t)B * q_len);
-  int slots = mla::plan_host(seq_lens, B, q_len, max_pages, page_size, num_splits, C, plan.data());
+  int slots = mla::plan_host(seq_lens, B, q_len, max_pages, page_size, num_splits, C, plan.data(), window);
   for (int u = 0; u < B * q_len; ++u) {
     unit_tile_begin[u] = plan[u].tile_begin;
     unit_tiles[u] = plan[u].tiles;
@@ -137,11 +144,13 @@ MLA_EXPORT mla_status_t mla_decode_plan_host(const int32_t* seq_lens, int B, int
   return MLA_OK;
 }
 
-MLA_EXPORT mla_status_t mla_decode(const void* q_nope, const void* q_pe, const void* kv_cache,
-                                   const int32_t* block_table, int max_pages, const int32_t* seq_lens,
-                                   int B, int q_len, int H, int num_pages, int page_size, float sm_scale,
-                                   int kv_dtype, float kv_scale, int num_splits, void* workspace,
-                                   size_t workspace_bytes, void* out, float* lse, mla_stream_t stream) {
+MLA_EXPORT mla_status_t mla_decode_ex(const void* q_nope, const void* q_pe, const void* kv_cache,
+                                      const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                                      int B, int q_len, int H, int num_pages, int page_size, float sm_scale,
+                                      int kv_dtype, float kv_scale, int num_splits, int window,
+                                      const float* sinks, void* workspace, size_t workspace_bytes, void* out,
+                                      float* lse, mla_stream_t stream) {
+  if (window < 0) return MLA_ERR_INVALID_ARG;
   mla_status_t st = check_shape(B, q_len, H, num_splits);
   if (st != MLA_OK) return st;
   st = check_geometry(B, q_len, max_pages, num_pages, page_size);
@@ -154,7 +163,8 @@ MLA_EXPORT mla_status_t mla_decode(const void* q_nope, const void* q_pe, const v
   if (!q_nope || !q_pe || !kv_cache || !block_table || !seq_lens || !workspace || !out)
     return MLA_ERR_INVALID_ARG;
   if (!aligned(q_nope, 16) || !aligned(q_pe, 16) || !aligned(kv_cache, 128) || !aligned(block_table, 16) ||
-      !aligned(seq_lens, 4) || !aligned(workspace, 256) || !aligned(out, 16) || (lse && !aligned(lse, 4)))
+      !aligned(seq_lens, 4) || !aligned(workspace, 256) || !aligned(out, 16) || (lse && !aligned(lse, 4)) ||
+      (sinks && !aligned(sinks, 4)))
     return MLA_ERR_INVALID_ARG;
   int C = 0;
   if (current_workers(&C) != cudaSuccess) return MLA_ERR_CUDA;
@@ -182,28 +192,41 @@ MLA_EXPORT mla_status_t mla_decode(const void* q_nope, const void* q_pe, const v
   p.ws = static_cast<uint8_t*>(workspace);
   p.out = static_cast<uint16_t*>(out);
   p.lse = lse;
+  p.window = window;
+  p.sinks = sinks;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // No host-side reset: each decode CTA writes its status word at exit and the reduce (which
   // always runs, after the decode) folds them into the call's status word.
   cudaError_t le = mla::launch_decode_tc(p, s);
   if (le != cudaSuccess) return MLA_ERR_CUDA;
-  if (mla::launch_splitk_reduce(p.ws, U, H, p.slots_cap, 2 * p.workers, p.out, lse, s, true) != cudaSuccess)
+  if (mla::launch_splitk_reduce(p.ws, U, H, p.slots_cap, 2 * p.workers, sinks, p.out, lse, s, true) != cudaSuccess)
     return MLA_ERR_CUDA;
   return MLA_OK;
 }
 
+MLA_EXPORT mla_status_t mla_decode(const void* q_nope, const void* q_pe, const void* kv_cache,
+                                   const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                                   int B, int q_len, int H, int num_pages, int page_size, float sm_scale,
+                                   int kv_dtype, float kv_scale, int num_splits, void* workspace,
+                                   size_t workspace_bytes, void* out, float* lse, mla_stream_t stream) {
+  return mla_decode_ex(q_nope, q_pe, kv_cache, block_table, max_pages, seq_lens, B, q_len, H, num_pages, page_size,
+                       sm_scale, kv_dtype, kv_scale, num_splits, 0, nullptr, workspace, workspace_bytes, out, lse,
+                       stream);
+}
+
 MLA_EXPORT mla_status_t mla_splitk_reduce(const void* workspace, size_t workspace_bytes, int B, int q_len,
-                                          int H, void* out, float* lse, mla_stream_t stream) {
+                                          int H, const float* sinks, void* out, float* lse, mla_stream_t stream) {
   mla_status_t st = check_shape(B, q_len, H, 0);
   if (st != MLA_OK) return st;
   if (B == 0) return MLA_OK;
   if (!workspace || !out) return MLA_ERR_INVALID_ARG;
-  if (!aligned(workspace, 256) || !aligned(out, 16) || (lse && !aligned(lse, 4))) return MLA_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256) || !aligned(out, 16) || (lse && !aligned(lse, 4)) || (sinks && !aligned(sinks, 4)))
+    return MLA_ERR_INVALID_ARG;
   if (workspace_bytes < mla::kHeaderBytes) return MLA_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (mla::launch_splitk_reduce(static_cast<uint8_t*>(const_cast<void*>(workspace)), B * q_len, H,
-                                slots_that_fit(workspace_bytes, H), 0, static_cast<uint16_t*>(out), lse, s,
+                                slots_that_fit(workspace_bytes, H), 0, sinks, static_cast<uint16_t*>(out), lse, s,
                                 false) != cudaSuccess)
     return MLA_ERR_CUDA;
   return MLA_OK;
@@ -218,4 +241,46 @@ MLA_EXPORT mla_status_t mla_decode_read_status(const void* workspace, uint32_t* 
   if (cudaStreamSynchronize(s) != cudaSuccess) return MLA_ERR_CUDA;
   *device_status = v;
   return v ? MLA_ERR_DEVICE_STATUS : MLA_OK;
+}
+
+MLA_EXPORT mla_status_t mla_kv_append(const void* latent, int64_t latent_stride, const void* rope, int64_t rope_stride,
+                                      const int64_t* slots, int T, void* kv_cache, int num_pages, int page_size,
+                                      int kv_dtype, float kv_scale, uint32_t* device_status, mla_stream_t stream) {
+  if (T < 0 || num_pages < 1) return MLA_ERR_INVALID_ARG;
+  if (page_size != 32 && page_size != 64) return MLA_ERR_UNSUPPORTED;
+  if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3 && kv_dtype != MLA_KV_NVFP4) return MLA_ERR_INVALID_ARG;
+  if (kv_dtype == MLA_KV_FP8_E4M3 && !(isfinite(kv_scale) && kv_scale > 0.f)) return MLA_ERR_INVALID_ARG;
+  if (T == 0) return MLA_OK;
+  if (!latent || !rope || !slots || !kv_cache) return MLA_ERR_INVALID_ARG;
+  if (latent_stride < 512 || rope_stride < 64 || latent_stride % 8 || rope_stride % 8) return MLA_ERR_INVALID_ARG;
+  if (!aligned(latent, 16) || !aligned(rope, 16) || !aligned(slots, 8) || !aligned(kv_cache, 128) ||
+      (device_status && !aligned(device_status, 4)))
+    return MLA_ERR_INVALID_ARG;
+  if (mla::launch_kv_append(static_cast<const uint16_t*>(latent), latent_stride, static_cast<const uint16_t*>(rope),
+                            rope_stride, slots, T, static_cast<uint8_t*>(kv_cache), (long long)num_pages * page_size,
+                            page_size, kv_dtype, kv_dtype == MLA_KV_FP8_E4M3 ? kv_scale : 1.f, device_status,
+                            reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+MLA_EXPORT mla_status_t mla_batched_gemv(const void* x, int64_t x_token_stride, int64_t x_head_stride,
+                                         const void* weight, void* out, int64_t out_token_stride,
+                                         int64_t out_head_stride, int T, int H, int N, int K,
+                                         uint32_t* device_status, mla_stream_t stream) {
+  if (T < 0 || H < 1 || N < 1 || K < 8 || K % 8) return MLA_ERR_INVALID_ARG;
+  if ((long long)H * N > 0x7fffffffLL || T > 0xffffff || H > 65535) return MLA_ERR_UNSUPPORTED;
+  if (T == 0) return MLA_OK;
+  if (!x || !weight || !out) return MLA_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(weight, 16) || !aligned(out, 16) || (device_status && !aligned(device_status, 4)))
+    return MLA_ERR_INVALID_ARG;
+  if (x_head_stride < K || x_head_stride % 8 || x_token_stride % 8 || x_token_stride < (int64_t)H * x_head_stride)
+    return MLA_ERR_INVALID_ARG;
+  if (out_head_stride < N || out_token_stride < 0) return MLA_ERR_INVALID_ARG;
+  cudaError_t e = mla::launch_batched_gemv(static_cast<const uint16_t*>(x), x_token_stride, x_head_stride,
+                                           static_cast<const uint16_t*>(weight), static_cast<uint16_t*>(out),
+                                           out_token_stride, out_head_stride, T, H, N, K, device_status,
+                                           reinterpret_cast<cudaStream_t>(stream));
+  if (e == cudaErrorInvalidValue) return MLA_ERR_INVALID_ARG;
+  return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }

@@ -63,6 +63,13 @@ MLA_HD int unit_visible(int seq_len_clamped, int q_len, int i) {
   return v < 0 ? 0 : v;
 }
 
+// Sliding window (window > 0): a query attends the last `window` of its visible positions,
+// [window_first, vis).  Its KV range is cut into 64-token tiles starting at the tile that
+// holds window_first (the rows before it are masked inside that tile).
+MLA_HD int window_first(int vis, int window) { return window > 0 && vis > window ? vis - window : 0; }
+MLA_HD int unit_tile0(int vis, int window) { return window_first(vis, window) / kTile; }
+MLA_HD int unit_tiles(int vis, int window) { return vis > 0 ? cdiv_i(vis, kTile) - unit_tile0(vis, window) : 0; }
+
 // ---- heuristic mode (num_splits == 0): contiguous, balanced tile ranges per worker ----
 // With N tiles and C workers, only C' = min(C, N) workers get work, so no range is empty;
 // worker c < C' owns global tiles [floor(c*N/C'), floor((c+1)*N/C')).  Callers pass C'.
@@ -74,11 +81,10 @@ MLA_HD int worker_of(long long t, long long N, int C) {
 }
 
 // ---- forced mode (num_splits > 0): each unit cut into ranges of span tiles ----
-MLA_HD int forced_span_tiles(int visible, int num_splits) {
-  if (visible <= 0) return 1;
-  int span_tok = cdiv_i(visible, num_splits);
-  return cdiv_i(span_tok, kTile);
-}
+// span = cdiv(tiles, num_splits) tiles.  Without a window, tiles = cdiv(visible, 64) and
+// this equals roundup(cdiv(visible, num_splits), 64) / 64 (nested ceilings compose); with
+// one, counting the unit's tiles keeps it at num_splits parts at most.
+MLA_HD int forced_span_tiles(int tiles, int num_splits) { return tiles > 0 ? cdiv_i(tiles, num_splits) : 1; }
 
 // One unit's share of the schedule.
 struct UnitPlan {
@@ -91,16 +97,18 @@ struct UnitPlan {
 // Host evaluation of the whole plan (the device kernels evaluate the same formulas with a
 // block-wide scan).  Returns the number of partial slots used.
 inline int plan_host(const int32_t* seq_lens, int B, int q_len, int max_pages, int page_size,
-                     int num_splits, int C, UnitPlan* plan) {
+                     int num_splits, int C, UnitPlan* plan, int window = 0) {
   const int U = B * q_len;
   long long N = 0;
   for (int u = 0; u < U; ++u) {
     int b = u / q_len, i = u % q_len;
     int L = clamp_seq_len(seq_lens[b], max_pages, page_size);
     int vis = unit_visible(L, q_len, i);
-    plan[u].tiles = cdiv_i(vis, kTile);
+    plan[u].tiles = unit_tiles(vis, window);
     if (num_splits > 0) {
-      plan[u].parts = plan[u].tiles ? cdiv_i(plan[u].tiles, forced_span_tiles(vis, num_splits)) : 0;
+      plan[u].parts = plan[u].tiles
+                          ? cdiv_i(plan[u].tiles, forced_span_tiles(plan[u].tiles, num_splits))
+                          : 0;
       plan[u].tile_begin = (int)N;  // first item index
       N += plan[u].parts;
     } else {

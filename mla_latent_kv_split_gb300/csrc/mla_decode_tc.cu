@@ -162,6 +162,7 @@ struct Smem {
   Bars bars;
   unsigned long long mchain[128];  // per row: (tile index + 1) << 32 | reference max bits
   int4 items[kItemRing];           // work items {u, tok_lo, tok_hi, slot}; tok_hi < 0 ends the list
+  int items_min[kItemRing];        // the item's unit's first attended position (sliding window)
   float ep_m[2][2][128];           // [item parity][warpgroup][row] reference max
   float ep_l[2][2][128];           // [item parity][warpgroup][row] row sum relative to it
   unsigned long long tmask[kStages];  // rows of the staged tile that are real, visible positions
@@ -181,7 +182,7 @@ __device__ __forceinline__ Smem& smem_ref(uint8_t* raw) {
 }
 
 // (page_size is 32 or 64: one or two pages per tile)
-__device__ __forceinline__ TileInfo tile_info(const DecodeParams& p, int b, int t0, int tok_hi) {
+__device__ __forceinline__ TileInfo tile_info(const DecodeParams& p, int b, int t0, int tok_hi, int tok_min) {
   TileInfo ti;
   const bool two = p.page_size == 32;
   const int shift = two ? 5 : 6;
@@ -202,6 +203,8 @@ __device__ __forceinline__ TileInfo tile_info(const DecodeParams& p, int b, int 
       if (ti.page_ok[j]) ti.rowmask |= (rows >= 64 ? ~0ull : ((1ull << rows) - 1)) << (j << shift);
     }
   }
+  // rows before the sliding window's first position
+  if (tok_min > t0) ti.rowmask &= tok_min - t0 >= 64 ? 0ull : ~((1ull << (tok_min - t0)) - 1);
   return ti;
 }
 __device__ __forceinline__ bool tile_needs_fixup(const TileInfo& ti) { return ti.rowmask != ~0ull; }
@@ -255,14 +258,15 @@ __device__ __forceinline__ bool chain_wait(const unsigned long long* slot, unsig
 // Takes work item k from the ring (every reader takes every item, in order): waits for it,
 // copies it and frees the slot.  Called by a whole warp (one arrive, after all lanes copied)
 // or by a single thread.  Returns 1 for an item, 0 at the end of the list, -1 on abort.
-__device__ __forceinline__ int item_take(const int4* ring, uint32_t b_full, uint32_t b_empty, int k,
-                                         volatile int* abort_flag, WorkItem& it, bool whole_warp) {
+__device__ __forceinline__ int item_take(const int4* ring, const int* ring_min, uint32_t b_full, uint32_t b_empty,
+                                         int k, volatile int* abort_flag, WorkItem& it, bool whole_warp) {
   const int s = k % kItemRing;
   if (!ptx::mbar_wait(b_full + 8 * s, (uint32_t)(k / kItemRing) & 1u, abort_flag)) return -1;
   const int4 v = ring[s];
+  const int tmin = ring_min[s];
   if (whole_warp) __syncwarp();
   if (!whole_warp || (threadIdx.x & 31) == 0) ptx::mbar_arrive(b_empty + 8 * s);
-  it = WorkItem{v.x, v.y, v.z, v.w};
+  it = WorkItem{v.x, v.y, v.z, v.w, tmin};
   return v.z >= 0 ? 1 : 0;
 }
 
@@ -432,18 +436,18 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
     bool dead = false;
     WorkItem it;
     for (int k_item = 0;; ++k_item) {
-      const int got = item_take(S.items, b_item_full, b_item_empty, k_item, abort_flag, it, true);
+      const int got = item_take(S.items, S.items_min, b_item_full, b_item_empty, k_item, abort_flag, it, true);
       if (got <= 0) {
         dead = got < 0;
         break;
       }
       const int b = it.u / p.q_len;
-      TileInfo ti_next = tile_info(p, b, it.tok_lo, it.tok_hi);
+      TileInfo ti_next = tile_info(p, b, it.tok_lo, it.tok_hi, it.tok_min);
       for (int t0 = it.tok_lo; t0 < it.tok_hi; t0 += kTileN, ++g) {
         // this tile's block-table entries were read one tile earlier, the next tile's are
         // read now, before waiting for the stage
         const TileInfo ti = ti_next;
-        if (t0 + kTileN < it.tok_hi) ti_next = tile_info(p, b, t0 + kTileN, it.tok_hi);
+        if (t0 + kTileN < it.tok_hi) ti_next = tile_info(p, b, t0 + kTileN, it.tok_hi, it.tok_min);
         const int st = g % kStages;
         if (g >= kStages && !ptx::mbar_wait(b_kv_empty + 8 * st, ((g / kStages) - 1) & 1, abort_flag)) {
           dead = true;
@@ -525,7 +529,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       bool dead = false;
       WorkItem it;
       for (int k_item = 0; !dead; ++k_item) {
-        if (item_take(S.items, b_item_full, b_item_empty, k_item, abort_flag, it, false) <= 0) break;
+        if (item_take(S.items, S.items_min, b_item_full, b_item_empty, k_item, abort_flag, it, false) <= 0) break;
         if (!ptx::mbar_wait(b_q_ready, n_item & 1, abort_flag)) break;
         ptx::tc_fence_after();
         const int nt = (it.tok_hi - it.tok_lo + kTileN - 1) / kTileN;
@@ -575,7 +579,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       bool dead = false;
       WorkItem it;
       for (int k_item = 0; !dead; ++k_item) {
-        if (item_take(S.items, b_item_full, b_item_empty, k_item, abort_flag, it, false) <= 0) break;
+        if (item_take(S.items, S.items_min, b_item_full, b_item_empty, k_item, abort_flag, it, false) <= 0) break;
         const int nt = (it.tok_hi - it.tok_lo + kTileN - 1) / kTileN;
         for (int t = 0; t < nt; ++t, ++g) {
           if (!ptx::mbar_wait(b_p_full + 8 * (g & 1), (g >> 1) & 1, abort_flag)) { dead = true; break; }
@@ -700,9 +704,9 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
     const int tq = (warp - kWarpSender0) * 32 + lane;
     // the first item's unit is known from the schedule: its Q loads overlap the item ring's
     // start and the first cache loads
-    if (wst.busy) load_q(WorkItem{wst.u0, 0, 0, -1});
+    if (wst.busy) load_q(WorkItem{wst.u0, 0, 0, -1, 0});
     for (int k_item = 0; !dead; ++k_item) {
-      const int got = item_take(S.items, b_item_full, b_item_empty, k_item, abort_flag, it, true);
+      const int got = item_take(S.items, S.items_min, b_item_full, b_item_empty, k_item, abort_flag, it, true);
       if (got <= 0) {
         dead = got < 0;
         break;
@@ -761,7 +765,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
     bool dead = false;
     WorkItem it;
     for (int k_item = 0; !dead; ++k_item) {
-      if (item_take(S.items, b_item_full, b_item_empty, k_item, abort_flag, it, true) <= 0) break;
+      if (item_take(S.items, S.items_min, b_item_full, b_item_empty, k_item, abort_flag, it, true) <= 0) break;
       const int b = it.u / p.q_len;
       const int nt = (it.tok_hi - it.tok_lo + kTileN - 1) / kTileN;
       const int g0 = g;
@@ -920,13 +924,26 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       ptx::tc_fence_after();
       const float ma = S.ep_m[par][0][row], mb = S.ep_m[par][1][row];
       const float la = S.ep_l[par][0][row], lb = S.ep_l[par][1][row];
-      const float m_fin = fmaxf(ma, mb);
-      const float l = (la > 0.f ? la * ptx::ex2_approx(ma - m_fin) : 0.f) + (lb > 0.f ? lb * ptx::ex2_approx(mb - m_fin) : 0.f);
+      float m_fin = fmaxf(ma, mb);
+      float l = (la > 0.f ? la * ptx::ex2_approx(ma - m_fin) : 0.f) + (lb > 0.f ? lb * ptx::ex2_approx(mb - m_fin) : 0.f);
+      // a head's sink logit (natural-log units of the scaled scores) joins the normaliser of
+      // a row written directly; split parts leave it to the combine
+      float o_sink = 1.f;  // O is relative to m_fin: weight of the tokens against the new max
+      if (it.slot < 0 && p.sinks != nullptr && row < p.H) {
+        const float sk = __ldg(p.sinks + row) * kLog2e;
+        if (sk > m_fin) {  // the sink becomes the reference (also when no token was seen)
+          o_sink = l > 0.f ? ptx::ex2_approx(m_fin - sk) : 0.f;
+          l = l * o_sink + 1.f;
+          m_fin = sk;
+        } else if (sk != -INFINITY) {
+          l += ptx::ex2_approx(sk - m_fin);
+        }
+      }
       const int i = it.u % p.q_len;
       const bool real = row < p.H;
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const float lse_v = l > 0.f ? (m_fin + __log2f(l)) * kLn2 : -INFINITY;
-      const float oscale = inv * p.kv_scale;
+      const float oscale = inv * o_sink * p.kv_scale;
       const size_t orow = ((size_t)b * p.q_len + i) * p.H + (real ? row : 0);
       const bool direct = it.slot < 0, partial = it.slot >= 0 && it.slot < p.slots_cap;
       // O leaves through shared memory and TMA tensor stores (16 columns x 16 rows per box):
@@ -1024,6 +1041,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
           ptx::bulk_prefetch_l2(p.q_pe + (size_t)nx.u * p.H * kRope, (uint32_t)p.H * kRope * 2);
         }
         S.items[s] = more ? make_int4(nx.u, nx.tok_lo, nx.tok_hi, nx.slot) : make_int4(0, 0, -1, -1);
+        S.items_min[s] = more ? nx.tok_min : 0;
         ptx::mbar_arrive(b_item_full + 8 * s);
         if (!more) break;
       }

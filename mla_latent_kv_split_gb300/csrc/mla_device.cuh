@@ -24,6 +24,8 @@ struct DecodeParams {
   uint8_t* ws;                // workspace
   uint16_t* out;              // [B, q_len, H, 512] bf16 bits
   float* lse;                 // [B, q_len, H] or nullptr
+  int window;                 // sliding window (0: none)
+  const float* sinks;         // [H] per-head sink logits or nullptr
 };
 
 // Status bits accumulate in a CTA-local word (shared memory) that the CTA stores at exit.
@@ -134,9 +136,10 @@ __device__ inline void compute_plan(const DecodeParams& p, PlanSmem& pl, int* sc
     if (L < p.q_len && i == 0) bad |= MLA_STATUS_SEQ_LT_QLEN;
     int vis = unit_visible(L, p.q_len, i);
     pl.vis[u] = vis;
-    int tiles = cdiv_i(vis, kTile);
-    pl.begin[u] = p.num_splits > 0 ? (tiles ? cdiv_i(tiles, forced_span_tiles(vis, p.num_splits)) : 0)
-                                   : tiles;
+    int tiles = unit_tiles(vis, p.window);
+    pl.begin[u] = p.num_splits > 0
+                      ? (tiles ? cdiv_i(tiles, forced_span_tiles(tiles, p.num_splits)) : 0)
+                      : tiles;
   }
   if (bad && write_plan) set_status(cta_status, bad);
   __syncthreads();
@@ -184,6 +187,7 @@ __device__ inline void compute_plan(const DecodeParams& p, PlanSmem& pl, int* sc
 // (or -1 = final output written directly).
 struct WorkItem {
   int u, tok_lo, tok_hi, slot;
+  int tok_min;  // the unit's first attended position (sliding window; 0 without one)
 };
 
 // Smallest index k in [0, n] with a[k] > x, for a non-decreasing a.
@@ -194,43 +198,6 @@ __device__ __forceinline__ int upper_bound_i(const int* a, int n, int x) {
     if (a[mid] <= x) lo = mid + 1; else hi = mid;
   }
   return lo;
-}
-
-// Iterates worker c's items in order, calling f(WorkItem).
-template <class F>
-__device__ inline void for_each_item(const DecodeParams& p, const PlanSmem& pl, int c, F&& f) {
-  const int U = p.B * p.q_len;
-  const int C = p.workers;
-  const int N = pl.N;
-  if (N <= 0) return;
-  if (p.num_splits > 0) {
-    for (int j = c; j < N; j += C) {
-      int u = upper_bound_i(pl.begin, U + 1, j) - 1;
-      int k = j - pl.begin[u];
-      int vis = pl.vis[u];
-      int span = forced_span_tiles(vis, p.num_splits);
-      int tiles = cdiv_i(vis, kTile);
-      int lo = k * span, hi = min((k + 1) * span, tiles);
-      WorkItem it{u, lo * kTile, min(hi * kTile, vis), pl.slot[u] >= 0 ? pl.slot[u] + k : -1};
-      f(it);
-    }
-  } else {
-    const int Ca = active_workers(N, C);
-    if (c >= Ca) return;
-    long long s = worker_begin(c, N, Ca), e = worker_begin(c + 1, N, Ca);
-    if (s >= e) return;
-    int u = upper_bound_i(pl.begin, U + 1, (int)s) - 1;
-    long long t = s;
-    while (t < e) {
-      while (pl.begin[u + 1] <= t) ++u;
-      int tb = pl.begin[u], te = pl.begin[u + 1];
-      int lo = (int)(t - tb), hi = (int)(min(e, (long long)te) - tb);
-      int slot = pl.slot[u] >= 0 ? pl.slot[u] + (c - worker_of(tb, N, Ca)) : -1;
-      WorkItem it{u, lo * kTile, min(hi * kTile, pl.vis[u]), slot};
-      f(it);
-      t = min(e, (long long)te);
-    }
-  }
 }
 
 // ---------------------------------------------------------------- cursor form
@@ -247,7 +214,7 @@ struct WorkerStart {
 
 __device__ inline WorkerStart worker_start(const DecodeParams& p, const PlanSmem& pl, int c) {
   const int U = p.B * p.q_len;
-  WorkerStart w{0, 0, 0, pl.N, 0, WorkItem{0, 0, 0, -1}};
+  WorkerStart w{0, 0, 0, pl.N, 0, WorkItem{0, 0, 0, -1, 0}};
   if (pl.N <= 0) return w;
   int first;
   int Ca = 0;
@@ -264,18 +231,19 @@ __device__ inline WorkerStart worker_start(const DecodeParams& p, const PlanSmem
   w.base0 = pl.begin[u];
   w.slot0 = pl.pref[u];
   w.busy = 1;
-  const int vis = pl.vis[u], tiles = cdiv_i(vis, kTile);
+  const int vis = pl.vis[u], tiles = unit_tiles(vis, p.window);
+  const int t0 = unit_tile0(vis, p.window), tmin = window_first(vis, p.window);
   if (p.num_splits > 0) {  // item `first` is part k of unit u
     const int k = first - w.base0;
-    const int span = forced_span_tiles(vis, p.num_splits);
+    const int span = forced_span_tiles(tiles, p.num_splits);
     const int lo = k * span, hi = min((k + 1) * span, tiles);
-    w.first = WorkItem{u, lo * kTile, min(hi * kTile, vis), pl.slot[u] >= 0 ? pl.slot[u] + k : -1};
+    w.first = WorkItem{u, (t0 + lo) * kTile, min((t0 + hi) * kTile, vis), pl.slot[u] >= 0 ? pl.slot[u] + k : -1, tmin};
   } else {  // tiles [first, end of the worker's range or of the unit)
     const long long e = worker_begin(c + 1, pl.N, Ca);
     const int lo = first - w.base0;
     const int hi = (int)(min(e, (long long)w.base0 + tiles) - w.base0);
-    w.first = WorkItem{u, lo * kTile, min(hi * kTile, vis),
-                       pl.slot[u] >= 0 ? pl.slot[u] + (c - worker_of(w.base0, pl.N, Ca)) : -1};
+    w.first = WorkItem{u, (t0 + lo) * kTile, min((t0 + hi) * kTile, vis),
+                       pl.slot[u] >= 0 ? pl.slot[u] + (c - worker_of(w.base0, pl.N, Ca)) : -1, tmin};
   }
   return w;
 }
@@ -324,8 +292,8 @@ __device__ inline bool next_item(const DecodeParams& p, int N, ItemCursor& k, Wo
     int vis, tiles, parts, span;
     for (;;) {
       vis = unit_visible_dev(p, k.u);
-      tiles = cdiv_i(vis, kTile);
-      span = forced_span_tiles(vis, p.num_splits);
+      tiles = unit_tiles(vis, p.window);
+      span = forced_span_tiles(tiles, p.num_splits);
       parts = tiles ? cdiv_i(tiles, span) : 0;
       if (k.ib + parts > k.j) break;
       k.sacc += parts > 1 ? parts : 0;
@@ -334,20 +302,24 @@ __device__ inline bool next_item(const DecodeParams& p, int N, ItemCursor& k, Wo
     }
     const int q = k.j - k.ib;
     const int lo = q * span, hi = min((q + 1) * span, tiles);
-    it = WorkItem{k.u, lo * kTile, min(hi * kTile, vis), parts > 1 ? k.sacc + q : -1};
+    const int t0 = unit_tile0(vis, p.window);
+    it = WorkItem{k.u, (t0 + lo) * kTile, min((t0 + hi) * kTile, vis), parts > 1 ? k.sacc + q : -1,
+                  window_first(vis, p.window)};
     k.j += p.workers;
     return true;
   }
   const int Ca = active_workers(N, p.workers);
   while (k.t < k.e) {
     const int vis = unit_visible_dev(p, k.u);
-    const int tiles = cdiv_i(vis, kTile);
+    const int tiles = unit_tiles(vis, p.window);
     const long long te = k.tb + tiles;
     const int parts = tiles ? worker_of(te - 1, N, Ca) - worker_of(k.tb, N, Ca) + 1 : 0;
     const bool emit = te > k.t;
     if (emit) {
       const int lo = (int)(k.t - k.tb), hi = (int)(min(k.e, te) - k.tb);
-      it = WorkItem{k.u, lo * kTile, min(hi * kTile, vis), parts > 1 ? k.sacc + (k.c - worker_of(k.tb, N, Ca)) : -1};
+      const int t0 = unit_tile0(vis, p.window);
+      it = WorkItem{k.u, (t0 + lo) * kTile, min((t0 + hi) * kTile, vis),
+                    parts > 1 ? k.sacc + (k.c - worker_of(k.tb, N, Ca)) : -1, window_first(vis, p.window)};
       k.t = min(k.e, te);
     }
     if (k.t >= te) {

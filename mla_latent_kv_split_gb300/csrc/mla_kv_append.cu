@@ -1,0 +1,135 @@
+// mla_kv_append.cu -- writes this step's new tokens into the paged latent cache, quantising
+// on the way in (tokenspeed "tokenspeed_mla.py", CuteDSLMLABackend.forward_decode: the new
+// tokens' latent and rope go to their cache locations before the decode reads them; metrale
+// "kv_cache_mla.rs", mla_cache_assemble and the NVFP4 / FP8 page layouts).
+//
+// One warp per token.  The token's 576 bf16 values [latent 512 | rope 64] are read as 16-byte
+// chunks; each lane owns whole chunks, so every global access is a full 16-byte vector.
+//   bf16 : 72 chunks of 8 values, copied.
+//   FP8  : 36 groups of 16 values -> 16 E4M3 codes of x / kv_scale (fp32 quotient).
+//   NVFP4: 36 groups of 16 values -> scale s = E4M3(amax / 6), 16 E2M1 codes of x / value(s)
+//          packed two per byte (element 2j in the low nibble of byte j), the scale byte in
+//          the page's scale section.  A group whose scale is 0 stores zero codes.
+// Conversions use the hardware's round-to-nearest-even, saturating (satfinite) converts.
+// The work is a few KB per token: HBM/latency-bound, sized as ceil(T / 8) blocks of 8 warps.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mla_decode.h"
+
+namespace mla {
+
+namespace {
+
+constexpr int kAppendThreads = 256;
+constexpr int kAppendWarps = kAppendThreads / 32;
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// Two values -> two E4M3 codes, `lo` in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// Eight values -> eight E2M1 codes in one word, element 2j in the low nibble of byte j.
+__device__ __forceinline__ uint32_t e2m1x8(const float* x) {
+  uint32_t d;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(d)
+      : "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]), "f"(x[7]));
+  return d;
+}
+
+// Value of one E4M3 code (exact: every E4M3 value is an f16 value).
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+  uint32_t h2;
+  const uint16_t c = (uint16_t)(code & 0xFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+  return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+}
+
+// 16 values of group g (0..35) of a token: groups 0..31 are latent, 32..35 rope.
+__device__ __forceinline__ void load_group(const uint16_t* lat, const uint16_t* rope, int g, float* x) {
+  const uint4* src = reinterpret_cast<const uint4*>(g < 32 ? lat + 16 * g : rope + 16 * (g - 32));
+  const uint4 a = __ldg(src), b = __ldg(src + 1);
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    x[2 * k] = bf16_lo(w[k]);
+    x[2 * k + 1] = bf16_hi(w[k]);
+  }
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kAppendThreads)
+mla_kv_append_kernel(const uint16_t* __restrict__ latent, long long latent_stride, const uint16_t* __restrict__ rope,
+                     long long rope_stride, const int64_t* __restrict__ slots, int T, uint8_t* __restrict__ cache,
+                     long long num_slots, int page_size, int kv_dtype, float kv_scale, uint32_t* status) {
+  const int t = blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const long long slot = __ldg(slots + t);
+  if (slot < 0) return;  // padding
+  if (slot >= num_slots) {
+    if (lane == 0 && status != nullptr) atomicOr(status, MLA_STATUS_SLOT_OUT_OF_RANGE);
+    return;
+  }
+  const uint16_t* lat = latent + (size_t)t * latent_stride;
+  const uint16_t* rp = rope + (size_t)t * rope_stride;
+  if (kv_dtype == MLA_KV_BF16) {
+    uint4* dst = reinterpret_cast<uint4*>(cache + (size_t)slot * (MLA_CACHE_DIM * 2));
+    for (int c = lane; c < 72; c += 32)
+      dst[c] = __ldg(reinterpret_cast<const uint4*>(c < 64 ? lat + 8 * c : rp + 8 * (c - 64)));
+    return;
+  }
+  for (int g = lane; g < 36; g += 32) {
+    float x[16];
+    load_group(lat, rp, g, x);
+    if (kv_dtype == MLA_KV_FP8_E4M3) {
+      uint32_t w[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        w[k] = e4m3x2(__fdiv_rn(x[4 * k], kv_scale), __fdiv_rn(x[4 * k + 1], kv_scale)) |
+               (e4m3x2(__fdiv_rn(x[4 * k + 2], kv_scale), __fdiv_rn(x[4 * k + 3], kv_scale)) << 16);
+      *reinterpret_cast<uint4*>(cache + (size_t)slot * MLA_CACHE_DIM + 16 * g) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+      float amax = 0.f;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(x[k]));
+      const uint32_t s_code = e4m3x2(__fdiv_rn(amax, 6.f), 0.f) & 0xFFu;
+      const float s = e4m3_value(s_code);
+      uint32_t d0 = 0u, d1 = 0u;
+      if (s > 0.f) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) x[k] = __fdiv_rn(x[k], s);
+        d0 = e2m1x8(x);
+        d1 = e2m1x8(x + 8);
+      }
+      const long long page = slot / page_size, row = slot - page * page_size;
+      uint8_t* base = cache + (size_t)page * ((size_t)page_size * (MLA_CACHE_DIM / 2 + MLA_CACHE_DIM / 16));
+      *reinterpret_cast<uint2*>(base + row * (MLA_CACHE_DIM / 2) + 8 * g) = make_uint2(d0, d1);
+      base[(size_t)page_size * (MLA_CACHE_DIM / 2) + row * (MLA_CACHE_DIM / 16) + g] = (uint8_t)s_code;
+    }
+  }
+}
+
+cudaError_t launch_kv_append(const uint16_t* latent, long long latent_stride, const uint16_t* rope,
+                             long long rope_stride, const int64_t* slots, int T, uint8_t* cache, long long num_slots,
+                             int page_size, int kv_dtype, float kv_scale, uint32_t* status, cudaStream_t stream) {
+  const int blocks = (T + kAppendWarps - 1) / kAppendWarps;
+  mla_kv_append_kernel<<<blocks, kAppendThreads, 0, stream>>>(latent, latent_stride, rope, rope_stride, slots, T,
+                                                              cache, num_slots, page_size, kv_dtype, kv_scale, status);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -5,7 +5,10 @@
 //   lse = log sum_s exp(lse_s);  out = sum_s exp(lse_s - lse) o_s.
 // evaluated in one pass with a running maximum (parts taken two at a time).  A (b, i) with
 // nothing visible gets out = 0 and lse = -inf; one with a single part was written by the
-// decode kernel and is skipped.  After a decode, the first CTA also folds the decode CTAs'
+// decode kernel and is skipped.  With per-head attention sinks (gpt-oss style: one extra
+// logit per head that takes part in the normaliser but has no value row), the sink joins
+// the combined normaliser here: lse' = log(exp(lse) + exp(sink_h)), out' = out *
+// exp(lse - lse'); a (b, i) with nothing visible then gets lse = sink_h.  After a decode, the first CTA also folds the decode CTAs'
 // status bits into the call's status word.
 //
 // One CTA of 256 threads per (unit, 8 heads): warp w takes one head, lane l its 16 output
@@ -26,7 +29,7 @@ constexpr int kPartGroup = 2;
 
 __global__ void __launch_bounds__(kReduceThreads, 4)
 mla_splitk_reduce_kernel(uint8_t* __restrict__ ws, int U, int H, int slots_cap, int status_ctas,
-                         uint16_t* __restrict__ out, float* __restrict__ lse) {
+                         const float* __restrict__ sinks, uint16_t* __restrict__ out, float* __restrict__ lse) {
   // Programmatic dependent launch: everything before this point overlaps the decode
   // kernel's tail; the plan and partials are read only after the decode has completed.
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -85,6 +88,17 @@ mla_splitk_reduce_kernel(uint8_t* __restrict__ ws, int U, int H, int slots_cap, 
       m = mn;
     }
   }
+  if (sinks != nullptr) {
+    const float sk = __ldg(sinks + h);
+    const float mn = fmaxf(m, sk);
+    if (mn != -INFINITY) {
+      const float sc = l > 0.f ? expf(m - mn) : 0.f;
+      l = l * sc + expf(sk - mn);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) acc[k] *= sc;
+      m = mn;
+    }
+  }
   const float inv = l > 0.f ? 1.f / l : 0.f;
   uint32_t pk[8];
 #pragma unroll
@@ -96,8 +110,8 @@ mla_splitk_reduce_kernel(uint8_t* __restrict__ ws, int U, int H, int slots_cap, 
   if (lse && lane == 0) lse[row] = l > 0.f ? m + logf(l) : -INFINITY;
 }
 
-cudaError_t launch_splitk_reduce(uint8_t* ws, int U, int H, int slots_cap, int status_ctas, uint16_t* out,
-                                 float* lse, cudaStream_t stream, bool pdl) {
+cudaError_t launch_splitk_reduce(uint8_t* ws, int U, int H, int slots_cap, int status_ctas, const float* sinks,
+                                 uint16_t* out, float* lse, cudaStream_t stream, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(U, (H + kReduceHeads - 1) / kReduceHeads);
   cfg.blockDim = dim3(kReduceThreads);
@@ -108,7 +122,7 @@ cudaError_t launch_splitk_reduce(uint8_t* ws, int U, int H, int slots_cap, int s
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, mla_splitk_reduce_kernel, ws, U, H, slots_cap, status_ctas, out, lse);
+  return cudaLaunchKernelEx(&cfg, mla_splitk_reduce_kernel, ws, U, H, slots_cap, status_ctas, sinks, out, lse);
 }
 
 }  // namespace mla

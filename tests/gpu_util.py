@@ -35,15 +35,18 @@ def to_device(inp: dict, device="cuda"):
     return d
 
 
-def run_decode(inp: dict, dev: dict | None = None, num_splits=None, workspace=None, out=None, lse=None):
+def run_decode(inp: dict, dev: dict | None = None, num_splits=None, workspace=None, out=None, lse=None,
+               window: int = 0, sinks=None):
     w = inp["workload"]
     dev = dev or to_device(inp)
     ns = w.num_splits if num_splits is None else num_splits
     if workspace is None:
         workspace = mb.alloc_workspace(w.B, w.q_len, w.H, ns)
+    d_sinks = None if sinks is None else torch.from_numpy(np.asarray(sinks, np.float32)).cuda()
     out, lse = mb.mla_decode(dev["q_nope"], dev["q_pe"], dev["cache"], dev["block_table"], dev["seq_lens"],
                              w.sm_scale, w.kv_dtype, inp["kv_scale"], ns, page_size=w.page_size,
-                             num_pages=inp["num_pages"], workspace=workspace, out=out, lse=lse)
+                             num_pages=inp["num_pages"], workspace=workspace, out=out, lse=lse,
+                             window=window, sinks=d_sinks)
     status = mb.mla_decode_read_status(workspace)
     torch.cuda.synchronize()
     o = out.float().cpu().double().numpy()
@@ -51,11 +54,12 @@ def run_decode(inp: dict, dev: dict | None = None, num_splits=None, workspace=No
     return o, l, status, workspace
 
 
-def oracle_ref(inp: dict, rows=None):
+def oracle_ref(inp: dict, rows=None, window: int = 0, sinks=None):
     w = inp["workload"]
     return oracle.mla_decode_ref(inp["q_nope"], inp["q_pe"], inp["cache"], inp["block_table"], inp["seq_lens"],
                                  w.sm_scale, kv_dtype=w.kv_dtype, kv_scale=inp["kv_scale"],
-                                 page_size=w.page_size, rows=rows)
+                                 page_size=w.page_size, rows=rows, window=window,
+                                 sinks=None if sinks is None else np.asarray(sinks, np.float64))
 
 
 def assert_close(out, lse, ref_out, ref_lse, rows=None, what=""):
@@ -73,6 +77,8 @@ def assert_close(out, lse, ref_out, ref_lse, rows=None, what=""):
         le = np.abs(lse[fin] - ref_lse[fin]).max()
         assert le <= LSE_ATOL, f"{what}: lse err {le:.3g}"
     assert np.all(out[~fin] == 0), f"{what}: empty rows must be 0"
+    empty = np.all(ref_out == 0, axis=-1)  # nothing visible (a finite sink still sets lse)
+    assert np.all(out[empty] == 0), f"{what}: rows with nothing visible must be 0"
     den = np.linalg.norm(ref_out)
     if den > 0:
         rel = np.linalg.norm(out - ref_out) / den

@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(L):
     for name in declared:
         assert hasattr(L, name), name
     assert set(mb.EXPORTED) <= set(declared)
-    assert L.mla_decode_abi_version() == 1
+    assert L.mla_decode_abi_version() == 2
     for code in range(6):
         assert L.mla_status_string(code).decode().startswith("MLA_")
 
@@ -69,15 +69,17 @@ def test_empty_batch_is_a_noop(L):
     assert _call(L, B=0, q_nope=None, q_pe=None, kv=None, bt=None, sl=None, ws=None, out=None, lse=None) == 0
 
 
-def _check_plan(seq_lens, q_len, ps, num_splits, C, max_pages=None):
+def _check_plan(seq_lens, q_len, ps, num_splits, C, max_pages=None, window=0):
     seq_lens = np.asarray(seq_lens, dtype=np.int32)
     if max_pages is None:
         max_pages = max(1, int(-(-max(int(seq_lens.max()), 1) // ps)))
-    pl = mb.mla_decode_plan_host(seq_lens, q_len, max_pages, ps, num_splits, C)
+    pl = mb.mla_decode_plan_host(seq_lens, q_len, max_pages, ps, num_splits, C, window=window)
     U = len(seq_lens) * q_len
     vis = np.array([oracle.visible_len(min(max(int(seq_lens[u // q_len]), 0), max_pages * ps), q_len, u % q_len)
                     for u in range(U)])
-    tiles = -(-vis // 64)
+    # 64-token tiles from the one holding the window's first position to the last visible one
+    first = np.array([oracle.window_range(int(v), window)[0] for v in vis])
+    tiles = np.where(vis > 0, -(-vis // 64) - first // 64, 0)
     assert np.array_equal(pl["tiles"], tiles)
     # slots: contiguous, disjoint, only for split units
     used = 0
@@ -91,8 +93,11 @@ def _check_plan(seq_lens, q_len, ps, num_splits, C, max_pages=None):
     assert used == pl["slots_used"]
     if num_splits > 0:
         for u in range(U):
-            if tiles[u]:
+            if tiles[u] and window == 0:
                 assert pl["parts"][u] == len(oracle.forced_split_ranges(int(vis[u]), num_splits))
+            elif tiles[u]:  # ranges of cdiv(tiles, num_splits) tiles: never more than num_splits
+                span = -(-int(tiles[u]) // num_splits)
+                assert pl["parts"][u] == -(-int(tiles[u]) // span) <= num_splits
     else:
         assert used <= 2 * C
         # brute force: assign tiles to workers by the balanced rule and count parts
@@ -138,3 +143,63 @@ def test_plan_clamps_and_negative_lengths(L):
     pl = _check_plan([-5, 10 ** 6, 3], 2, 64, 0, 4, max_pages=2)
     assert pl["tiles"][0] == 0 and pl["tiles"][1] == 0  # seq_len -5 -> nothing visible
     assert pl["tiles"][2] == 2 and pl["tiles"][3] == 2  # clamped to 128: 127 and 128 visible
+
+
+@pytest.mark.parametrize("window", [1, 63, 64, 65, 200, 5000])
+@pytest.mark.parametrize("num_splits", [0, 2, 3])
+def test_plan_with_sliding_window(L, window, num_splits):
+    rng = np.random.default_rng(window + num_splits)
+    for trial in range(4):
+        B = int(rng.integers(1, 20))
+        q_len = int(rng.integers(1, 4))
+        seq = rng.integers(0, 3000, size=B)
+        _check_plan(seq, q_len, 64 if trial % 2 else 32, num_splits, int(rng.integers(1, 80)), window=window)
+
+
+def test_window_and_sink_arguments_validated(L):
+    args = [16, 16, 128, 16, 4, 16, 1, 1, 16, 4, 64, 0.1, 0, 1.0, 0]
+    assert L.mla_decode_ex(*args, -1, None, 256, 1 << 30, 16, 16, None) == 1  # negative window
+    assert L.mla_decode_ex(*args, 0, 18, 256, 1 << 30, 16, 16, None) == 1  # misaligned sinks
+    assert L.mla_decode_ex(*args[:6], 0, *args[7:], 5, None, None, 0, None, None, None) == 0  # B = 0
+    i32 = ctypes.POINTER(ctypes.c_int32)
+    z = (ctypes.c_int32 * 1)()
+    sl = (ctypes.c_int32 * 1)(10)
+    assert L.mla_decode_plan_host(sl, 1, 1, 1, 64, 0, -3, 4, z, z, z, z, z) == 1
+
+
+def test_kv_append_arguments_validated(L):
+    P = 1 << 20  # any 128-byte aligned non-null value: nothing is launched on these paths
+    ok = dict(lat=P, ls=576, rope=P + 1024, rs=576, slots=P, T=4, cache=P, num_pages=2, ps=64, kd=0, scale=1.0,
+              status=None)
+
+    def call(**over):
+        a = dict(ok)
+        a.update(over)
+        return L.mla_kv_append(a["lat"], a["ls"], a["rope"], a["rs"], a["slots"], a["T"], a["cache"], a["num_pages"],
+                               a["ps"], a["kd"], a["scale"], a["status"], None)
+
+    for over, code in [(dict(T=-1), 1), (dict(num_pages=0), 1), (dict(ps=16), 2), (dict(kd=5), 1),
+                       (dict(kd=1, scale=0.0), 1), (dict(kd=1, scale=float("nan")), 1), (dict(lat=None), 1),
+                       (dict(slots=None), 1), (dict(ls=511), 1), (dict(rs=60), 1), (dict(ls=580), 1),
+                       (dict(lat=P + 2), 1), (dict(rope=P + 8), 1), (dict(slots=P + 4), 1), (dict(cache=P + 64), 1),
+                       (dict(status=P + 2), 1)]:
+        assert call(**over) == code, over
+    assert call(T=0, lat=None, rope=None, slots=None, cache=None) == 0
+
+
+def test_batched_gemv_arguments_validated(L):
+    P = 1 << 20
+    ok = dict(x=P, xt=128 * 192, xh=192, w=P, out=P, ot=128 * 512, oh=512, T=4, H=128, N=512, K=128, status=None)
+
+    def call(**over):
+        a = dict(ok)
+        a.update(over)
+        return L.mla_batched_gemv(a["x"], a["xt"], a["xh"], a["w"], a["out"], a["ot"], a["oh"], a["T"], a["H"],
+                                  a["N"], a["K"], a["status"], None)
+
+    for over, code in [(dict(T=-1), 1), (dict(H=0), 1), (dict(N=0), 1), (dict(K=4), 1), (dict(K=100), 1),
+                       (dict(x=None), 1), (dict(w=None), 1), (dict(out=None), 1), (dict(x=P + 8), 1),
+                       (dict(w=P + 2), 1), (dict(out=P + 4), 1), (dict(xh=120), 1), (dict(xh=196), 1),
+                       (dict(xt=100), 1), (dict(oh=500), 1), (dict(H=70000), 2), (dict(status=P + 1), 1)]:
+        assert call(**over) == code, over
+    assert call(T=0, x=None, w=None, out=None) == 0
