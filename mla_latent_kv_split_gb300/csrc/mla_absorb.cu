@@ -10,8 +10,8 @@
 // tcgen05 MMA (M = 128) and the tokens its N side (16..256), so a decode step's few tokens
 // still fill the tensor core's M dimension and every weight byte is read once per token
 // tile.  TMA brings 64-column (128-byte, 128-byte-swizzled) K chunks of both operands into
-// a ring of stages; one thread issues the MMAs into TMEM; the four warps read the
-// accumulator back (lane = weight row) and store bf16.  Bound by HBM for decode-sized T
+// a ring of up to eight stages (all of K at decode sizes); one thread issues the MMAs
+// into TMEM; the four warps read the accumulator back (lane = weight row) and store bf16.  Bound by HBM for decode-sized T
 // (the weights dominate), by the tensor pipe only for thousands of tokens.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -27,7 +27,8 @@ namespace gemv {
 constexpr int kThreads = 128;
 constexpr int kBlockM = 128;     // weight rows per CTA
 constexpr int kBlockK = 64;      // bf16 columns per K chunk: one 128-byte swizzle row
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 8;
+constexpr uint32_t kStageBudget = 200 * 1024;  // shared memory for the stage ring
 constexpr int kMaxTokens = 256;  // tokens per CTA (MMA N)
 constexpr uint32_t kABytes = kBlockM * kBlockK * 2;
 
@@ -175,7 +176,10 @@ cudaError_t launch_batched_gemv(const uint16_t* x, long long x_token_stride, lon
   if (!fn) return cudaErrorNotSupported;
   const int tt = gemv_token_tile(T);
   const int nk = (K + gemv::kBlockK - 1) / gemv::kBlockK;
-  const int stages = nk < gemv::kMaxStages ? nk : gemv::kMaxStages;
+  // as many K chunks in flight as fit: the whole K extent for the MLA shapes at decode sizes
+  int stages = (int)(gemv::kStageBudget / gemv::stage_bytes(tt));
+  if (stages > gemv::kMaxStages) stages = gemv::kMaxStages;
+  if (stages > nk) stages = nk;
   CUtensorMap tm_w, tm_x;
   {
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)H * N};

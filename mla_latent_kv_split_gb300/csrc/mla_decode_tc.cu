@@ -345,8 +345,7 @@ constexpr bool decode_in_senders() { return KV == MLA_KV_FP8_E4M3; }
 template <int KV>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope,
-                     const __grid_constant__ CUtensorMap tm_out, const __grid_constant__ CUtensorMap tm_part,
-                     const DecodeParams p) {
+                     const __grid_constant__ CUtensorMap tm_out, const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   Smem& S = smem_ref(smem_raw);
   const int tid = threadIdx.x;
@@ -946,11 +945,12 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       const float oscale = inv * o_sink * p.kv_scale;
       const size_t orow = ((size_t)b * p.q_len + i) * p.H + (real ? row : 0);
       const bool direct = it.slot < 0, partial = it.slot >= 0 && it.slot < p.slots_cap;
-      // O leaves through shared memory and TMA tensor stores (16 columns x 16 rows per box):
-      // scattered per-thread global stores would cost one memory request per row.
-      const CUtensorMap* tmap = direct ? &tm_out : &tm_part;
-      const int row0 = (direct ? it.u : it.slot) * p.H + 32 * q;
-      const bool store = direct || partial;
+      // A final output leaves through shared memory and TMA tensor stores (16 columns x 16
+      // rows per box): a thread's row is not contiguous with its neighbours' in [U, H, 512].
+      // A split partial is stored straight from registers: in the workspace's quad-major
+      // layout a warp's 32 rows of one column quad are 512 contiguous bytes, so the stores
+      // need no staging and the next item's P.V can start as soon as O has been read.
+      const int row0 = it.u * p.H + 32 * q;
       // The worker's last item (the ring's next entry is the end marker): the cache stages
       // are idle, so each chunk gets a staging buffer of its own there and all stores are in
       // flight together.  Otherwise one 2 KB buffer per warp, reused chunk after chunk.
@@ -961,11 +961,25 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       }
       last = __all_sync(0xffffffffu, last);
       uint8_t* const stg0 = last ? S.stage[0] + sw * 16384 : S.ostage[sw];
+      float* const part =
+          reinterpret_cast<float*>(p.ws + partial_o_offset()) + ((size_t)it.slot * 128 * p.H + row) * 4;
+      const uint64_t pol_keep = ptx::l2_policy_evict_last();  // read again by the combine
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
         uint32_t r[16];
         ptx::tmem_ld16(t_o + 128 * wg + 16 * c, r);
         ptx::tmem_ld_wait();
+        if (!direct) {
+          if (partial && real) {
+            const int quad0 = (256 * (int)cr + 128 * wg + 16 * c) >> 2;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              ptx::st_global_v4_hint(part + (size_t)(quad0 + k) * p.H * 4, __uint_as_float(r[4 * k]) * oscale,
+                                     __uint_as_float(r[4 * k + 1]) * oscale, __uint_as_float(r[4 * k + 2]) * oscale,
+                                     __uint_as_float(r[4 * k + 3]) * oscale, pol_keep);
+          }
+          continue;
+        }
         uint8_t* const stg = last ? stg0 + 2048 * c : stg0;
         const uint32_t stg_a = ptx::smem_u32(stg);
         if (!last) {  // the previous chunk's stores (this item's or the last item's) have read the buffer
@@ -973,33 +987,21 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
           __syncwarp();
         }
         const int br = lane & 15;
-        if (direct) {
-          uint8_t* rowp = stg + (lane >> 4) * 512 + br * 32;
+        uint8_t* rowp = stg + (lane >> 4) * 512 + br * 32;
 #pragma unroll
-          for (int k = 0; k < 2; ++k)
-            *reinterpret_cast<uint4*>(rowp + ((k ^ ((br >> 2) & 1)) * 16)) =
-                make_uint4(ptx::pack_bf16x2(__uint_as_float(r[8 * k + 0]) * oscale, __uint_as_float(r[8 * k + 1]) * oscale),
-                           ptx::pack_bf16x2(__uint_as_float(r[8 * k + 2]) * oscale, __uint_as_float(r[8 * k + 3]) * oscale),
-                           ptx::pack_bf16x2(__uint_as_float(r[8 * k + 4]) * oscale, __uint_as_float(r[8 * k + 5]) * oscale),
-                           ptx::pack_bf16x2(__uint_as_float(r[8 * k + 6]) * oscale, __uint_as_float(r[8 * k + 7]) * oscale));
-        } else {
-          uint8_t* rowp = stg + (lane >> 4) * 1024 + br * 64;
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            *reinterpret_cast<float4*>(rowp + ((k ^ ((br >> 1) & 3)) * 16)) =
-                make_float4(__uint_as_float(r[4 * k]) * oscale, __uint_as_float(r[4 * k + 1]) * oscale,
-                            __uint_as_float(r[4 * k + 2]) * oscale, __uint_as_float(r[4 * k + 3]) * oscale);
-        }
+        for (int k = 0; k < 2; ++k)
+          *reinterpret_cast<uint4*>(rowp + ((k ^ ((br >> 2) & 1)) * 16)) =
+              make_uint4(ptx::pack_bf16x2(__uint_as_float(r[8 * k + 0]) * oscale, __uint_as_float(r[8 * k + 1]) * oscale),
+                         ptx::pack_bf16x2(__uint_as_float(r[8 * k + 2]) * oscale, __uint_as_float(r[8 * k + 3]) * oscale),
+                         ptx::pack_bf16x2(__uint_as_float(r[8 * k + 4]) * oscale, __uint_as_float(r[8 * k + 5]) * oscale),
+                         ptx::pack_bf16x2(__uint_as_float(r[8 * k + 6]) * oscale, __uint_as_float(r[8 * k + 7]) * oscale));
         ptx::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0 && store) {
+        if (lane == 0) {
           const int x = 256 * (int)cr + 128 * wg + 16 * c;
 #pragma unroll
           for (int h = 0; h < 2; ++h)
-            if (32 * q + 16 * h < p.H) {
-              if (direct) ptx::tma_store_2d(tmap, stg_a + h * 512, x, row0 + 16 * h);
-              else ptx::tma_store_2d_hint(tmap, stg_a + h * 1024, x, row0 + 16 * h, ptx::l2_policy_evict_last());
-            }
+            if (32 * q + 16 * h < p.H) ptx::tma_store_2d(&tm_out, stg_a + h * 512, x, row0 + 16 * h);
           ptx::bulk_commit();
         }
       }
@@ -1140,42 +1142,36 @@ int tc_max_clusters() {
 }
 
 template <int KV>
-static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o, const CUtensorMap& w,
-                             const DecodeParams& p, cudaStream_t stream) {
+static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o, const DecodeParams& p,
+                             cudaStream_t stream) {
   auto kern = tc::mla_decode_tc_kernel<KV>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem_bytes());
   if (e != cudaSuccess) return e;
-  kern<<<2 * p.workers, tc::kThreads, tc_smem_bytes(), stream>>>(a, b, o, w, p);
+  kern<<<2 * p.workers, tc::kThreads, tc_smem_bytes(), stream>>>(a, b, o, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t stream) {
   static_assert(sizeof(tc::Smem) + 1024 <= 227 * 1024, "shared memory budget");
-  CUtensorMap tm_lat, tm_rope, tm_out, tm_part;
+  CUtensorMap tm_lat, tm_rope, tm_out;
   memset(&tm_lat, 0, sizeof(tm_lat));
   memset(&tm_rope, 0, sizeof(tm_rope));
-  // outputs: [B*q_len*H, 512] bf16 and the partials [slots*H, 512] fp32, 16 x 16 boxes
+  // output: [B*q_len*H, 512] bf16, 16 x 16 boxes
   const int units = p.B * p.q_len;
   if (!encode_rows_map(&tm_out, p.out, (size_t)units * p.H, 2, CU_TENSOR_MAP_SWIZZLE_32B)) return cudaErrorInvalidValue;
-  if (p.slots_cap > 0) {
-    if (!encode_rows_map(&tm_part, p.ws + partial_o_offset(), (size_t)p.slots_cap * p.H, 4, CU_TENSOR_MAP_SWIZZLE_64B))
-      return cudaErrorInvalidValue;
-  } else {
-    tm_part = tm_out;  // never stored through: no item has a partial slot
-  }
   if (p.kv_dtype == MLA_KV_BF16) {
     if (!encode_cache_map(&tm_lat, p.cache, p.num_pages, p.page_size, 64, 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_cache_map(&tm_rope, p.cache, p.num_pages, p.page_size, 32, 2, CU_TENSOR_MAP_SWIZZLE_64B))
       return cudaErrorInvalidValue;
-    return launch_tc<MLA_KV_BF16>(tm_lat, tm_rope, tm_out, tm_part, p, stream);
+    return launch_tc<MLA_KV_BF16>(tm_lat, tm_rope, tm_out, p, stream);
   }
   if (p.kv_dtype == MLA_KV_FP8_E4M3) {
     if (!encode_cache_map(&tm_lat, p.cache, p.num_pages, p.page_size, 256, 1, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_cache_map(&tm_rope, p.cache, p.num_pages, p.page_size, 32, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
-    return launch_tc<MLA_KV_FP8_E4M3>(tm_lat, tm_rope, tm_out, tm_part, p, stream);
+    return launch_tc<MLA_KV_FP8_E4M3>(tm_lat, tm_rope, tm_out, p, stream);
   }
-  return launch_tc<MLA_KV_NVFP4>(tm_lat, tm_rope, tm_out, tm_part, p, stream);
+  return launch_tc<MLA_KV_NVFP4>(tm_lat, tm_rope, tm_out, p, stream);
 }
 
 }  // namespace mla

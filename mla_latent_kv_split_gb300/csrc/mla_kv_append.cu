@@ -3,15 +3,15 @@
 // tokens' latent and rope go to their cache locations before the decode reads them; metrale
 // "kv_cache_mla.rs", mla_cache_assemble and the NVFP4 / FP8 page layouts).
 //
-// One warp per token.  The token's 576 bf16 values [latent 512 | rope 64] are read as 16-byte
-// chunks; each lane owns whole chunks, so every global access is a full 16-byte vector.
-//   bf16 : 72 chunks of 8 values, copied.
-//   FP8  : 36 groups of 16 values -> 16 E4M3 codes of x / kv_scale (fp32 quotient).
-//   NVFP4: 36 groups of 16 values -> scale s = E4M3(amax / 6), 16 E2M1 codes of x / value(s)
-//          packed two per byte (element 2j in the low nibble of byte j), the scale byte in
-//          the page's scale section.  A group whose scale is 0 stores zero codes.
+// One thread per 16-value group: a token is 36 groups (32 latent, 4 rope), a block of 288
+// threads takes 8 tokens, so a warp reads 32 consecutive groups (1 KB) of one token.
+//   bf16 : the group's 32 bytes copied.
+//   FP8  : 16 E4M3 codes of x / kv_scale (fp32 quotient), one 16-byte store.
+//   NVFP4: scale s = E4M3(amax / 6), 16 E2M1 codes of x / value(s) packed two per byte
+//          (element 2j in the low nibble of byte j, one 8-byte store), the scale byte in the
+//          page's scale section.  A group whose scale is 0 stores zero codes.
 // Conversions use the hardware's round-to-nearest-even, saturating (satfinite) converts.
-// The work is a few KB per token: HBM/latency-bound, sized as ceil(T / 8) blocks of 8 warps.
+// HBM-bound; at a decode step's few hundred tokens, launch-latency-bound.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -22,8 +22,9 @@ namespace mla {
 
 namespace {
 
-constexpr int kAppendThreads = 256;
-constexpr int kAppendWarps = kAppendThreads / 32;
+constexpr int kGroups = 36;                      // 16-value groups per 576-value token
+constexpr int kAppendTokens = 8;                 // tokens per block
+constexpr int kAppendThreads = kGroups * kAppendTokens;
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
@@ -57,76 +58,71 @@ __device__ __forceinline__ float e4m3_value(uint32_t code) {
   return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
 }
 
-// 16 values of group g (0..35) of a token: groups 0..31 are latent, 32..35 rope.
-__device__ __forceinline__ void load_group(const uint16_t* lat, const uint16_t* rope, int g, float* x) {
-  const uint4* src = reinterpret_cast<const uint4*>(g < 32 ? lat + 16 * g : rope + 16 * (g - 32));
-  const uint4 a = __ldg(src), b = __ldg(src + 1);
-  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    x[2 * k] = bf16_lo(w[k]);
-    x[2 * k + 1] = bf16_hi(w[k]);
-  }
-}
-
 }  // namespace
 
 __global__ void __launch_bounds__(kAppendThreads)
 mla_kv_append_kernel(const uint16_t* __restrict__ latent, long long latent_stride, const uint16_t* __restrict__ rope,
                      long long rope_stride, const int64_t* __restrict__ slots, int T, uint8_t* __restrict__ cache,
                      long long num_slots, int page_size, int kv_dtype, float kv_scale, uint32_t* status) {
-  const int t = blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kAppendTokens + threadIdx.x / kGroups;
+  const int g = threadIdx.x % kGroups;
   if (t >= T) return;
   const long long slot = __ldg(slots + t);
   if (slot < 0) return;  // padding
   if (slot >= num_slots) {
-    if (lane == 0 && status != nullptr) atomicOr(status, MLA_STATUS_SLOT_OUT_OF_RANGE);
+    if (g == 0 && status != nullptr) atomicOr(status, MLA_STATUS_SLOT_OUT_OF_RANGE);
     return;
   }
   const uint16_t* lat = latent + (size_t)t * latent_stride;
   const uint16_t* rp = rope + (size_t)t * rope_stride;
+  const uint4* src = reinterpret_cast<const uint4*>(g < 32 ? lat + 16 * g : rp + 16 * (g - 32));
+  const uint4 a = __ldg(src), b = __ldg(src + 1);
   if (kv_dtype == MLA_KV_BF16) {
-    uint4* dst = reinterpret_cast<uint4*>(cache + (size_t)slot * (MLA_CACHE_DIM * 2));
-    for (int c = lane; c < 72; c += 32)
-      dst[c] = __ldg(reinterpret_cast<const uint4*>(c < 64 ? lat + 8 * c : rp + 8 * (c - 64)));
+    uint4* dst = reinterpret_cast<uint4*>(cache + (size_t)slot * (MLA_CACHE_DIM * 2) + 32 * g);
+    dst[0] = a;
+    dst[1] = b;
     return;
   }
-  for (int g = lane; g < 36; g += 32) {
-    float x[16];
-    load_group(lat, rp, g, x);
-    if (kv_dtype == MLA_KV_FP8_E4M3) {
-      uint32_t w[4];
+  float x[16];
+  {
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        w[k] = e4m3x2(__fdiv_rn(x[4 * k], kv_scale), __fdiv_rn(x[4 * k + 1], kv_scale)) |
-               (e4m3x2(__fdiv_rn(x[4 * k + 2], kv_scale), __fdiv_rn(x[4 * k + 3], kv_scale)) << 16);
-      *reinterpret_cast<uint4*>(cache + (size_t)slot * MLA_CACHE_DIM + 16 * g) = make_uint4(w[0], w[1], w[2], w[3]);
-    } else {
-      float amax = 0.f;
-#pragma unroll
-      for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(x[k]));
-      const uint32_t s_code = e4m3x2(__fdiv_rn(amax, 6.f), 0.f) & 0xFFu;
-      const float s = e4m3_value(s_code);
-      uint32_t d0 = 0u, d1 = 0u;
-      if (s > 0.f) {
-#pragma unroll
-        for (int k = 0; k < 16; ++k) x[k] = __fdiv_rn(x[k], s);
-        d0 = e2m1x8(x);
-        d1 = e2m1x8(x + 8);
-      }
-      const long long page = slot / page_size, row = slot - page * page_size;
-      uint8_t* base = cache + (size_t)page * ((size_t)page_size * (MLA_CACHE_DIM / 2 + MLA_CACHE_DIM / 16));
-      *reinterpret_cast<uint2*>(base + row * (MLA_CACHE_DIM / 2) + 8 * g) = make_uint2(d0, d1);
-      base[(size_t)page_size * (MLA_CACHE_DIM / 2) + row * (MLA_CACHE_DIM / 16) + g] = (uint8_t)s_code;
+    for (int k = 0; k < 8; ++k) {
+      x[2 * k] = bf16_lo(w[k]);
+      x[2 * k + 1] = bf16_hi(w[k]);
     }
   }
+  if (kv_dtype == MLA_KV_FP8_E4M3) {
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      w[k] = e4m3x2(__fdiv_rn(x[4 * k], kv_scale), __fdiv_rn(x[4 * k + 1], kv_scale)) |
+             (e4m3x2(__fdiv_rn(x[4 * k + 2], kv_scale), __fdiv_rn(x[4 * k + 3], kv_scale)) << 16);
+    *reinterpret_cast<uint4*>(cache + (size_t)slot * MLA_CACHE_DIM + 16 * g) = make_uint4(w[0], w[1], w[2], w[3]);
+    return;
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(x[k]));
+  const uint32_t s_code = e4m3x2(__fdiv_rn(amax, 6.f), 0.f) & 0xFFu;
+  const float sv = e4m3_value(s_code);
+  uint32_t d0 = 0u, d1 = 0u;
+  if (sv > 0.f) {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) x[k] = __fdiv_rn(x[k], sv);
+    d0 = e2m1x8(x);
+    d1 = e2m1x8(x + 8);
+  }
+  const long long page = slot / page_size, row = slot - page * page_size;
+  uint8_t* base = cache + (size_t)page * ((size_t)page_size * (MLA_CACHE_DIM / 2 + MLA_CACHE_DIM / 16));
+  *reinterpret_cast<uint2*>(base + row * (MLA_CACHE_DIM / 2) + 8 * g) = make_uint2(d0, d1);
+  base[(size_t)page_size * (MLA_CACHE_DIM / 2) + row * (MLA_CACHE_DIM / 16) + g] = (uint8_t)s_code;
 }
 
 cudaError_t launch_kv_append(const uint16_t* latent, long long latent_stride, const uint16_t* rope,
                              long long rope_stride, const int64_t* slots, int T, uint8_t* cache, long long num_slots,
                              int page_size, int kv_dtype, float kv_scale, uint32_t* status, cudaStream_t stream) {
-  const int blocks = (T + kAppendWarps - 1) / kAppendWarps;
+  const int blocks = (T + kAppendTokens - 1) / kAppendTokens;
   mla_kv_append_kernel<<<blocks, kAppendThreads, 0, stream>>>(latent, latent_stride, rope, rope_stride, slots, T,
                                                               cache, num_slots, page_size, kv_dtype, kv_scale, status);
   return cudaGetLastError();

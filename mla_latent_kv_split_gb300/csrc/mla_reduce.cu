@@ -11,10 +11,12 @@
 // exp(lse - lse'); a (b, i) with nothing visible then gets lse = sink_h.  After a decode, the first CTA also folds the decode CTAs'
 // status bits into the call's status word.
 //
-// One CTA of 256 threads per (unit, 8 heads): warp w takes one head, lane l its 16 output
-// columns [16 l, 16 l + 16), so a part's row of a head is one coalesced 2 KB read.  Every
-// load of a group of parts is issued before any is used: a part group costs one memory
-// round trip, and the whole grid (units x H / 8 CTAs) is resident at once.
+// One CTA of 256 threads per (unit, 32 heads, 128 columns): lane = head, warp = one 16-column
+// group.  The partials are stored column-quad-major ([slot][128][H][4] fp32), so for one
+// quad a warp's 32 heads are 512 contiguous bytes; each thread reads its 16 columns as four
+// such coalesced loads per part and writes its 32 output bytes whole.  Every load of a
+// group of parts is issued before any is used: a part group costs one memory round trip,
+// and the whole grid (units x H/32 x 4 CTAs) is resident at once.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -24,7 +26,8 @@
 namespace mla {
 
 constexpr int kReduceThreads = 256;
-constexpr int kReduceHeads = kReduceThreads / 32;
+constexpr int kReduceHeads = 32;                     // lanes
+constexpr int kReduceColGroups = kReduceThreads / 32;  // warps: 16 columns each
 constexpr int kPartGroup = 2;
 
 __global__ void __launch_bounds__(kReduceThreads, 4)
@@ -33,15 +36,16 @@ mla_splitk_reduce_kernel(uint8_t* __restrict__ ws, int U, int H, int slots_cap, 
   // Programmatic dependent launch: everything before this point overlaps the decode
   // kernel's tail; the plan and partials are read only after the decode has completed.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (status_ctas > 0 && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < 32) {
+  if (status_ctas > 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x < 32) {
     // the call's status word: the OR of every decode CTA's status bits
     unsigned bits = 0;
     for (int c = threadIdx.x; c < status_ctas; c += 32) bits |= reinterpret_cast<const unsigned*>(ws + kCtaStatusOffset)[c];
     bits = __reduce_or_sync(0xffffffffu, bits);
     if (threadIdx.x == 0) *reinterpret_cast<unsigned*>(ws) = bits;
   }
-  const int u = blockIdx.x, lane = threadIdx.x & 31;
-  const int h = blockIdx.y * kReduceHeads + (threadIdx.x >> 5);
+  const int u = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int h = blockIdx.y * kReduceHeads + lane;
+  const int col0 = 128 * blockIdx.z + 16 * warp;  // this thread's 16 output columns
   if (h >= H) return;
   const int2 pl = reinterpret_cast<const int2*>(ws + kPlanOffset)[u];
   const int parts = pl.x, slot = pl.y;
@@ -60,10 +64,11 @@ mla_splitk_reduce_kernel(uint8_t* __restrict__ ws, int U, int H, int slots_cap, 
 #pragma unroll
       for (int j = 0; j < kPartGroup; ++j) {
         const bool ok = s0 + j < parts;
-        const size_t r = (size_t)(slot + s0 + j) * H + h;
-        ls[j] = ok ? pls[r] : -INFINITY;
+        const size_t r = (size_t)(slot + s0 + j);
+        ls[j] = ok ? pls[r * H + h] : -INFINITY;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) v[j][k] = ok ? po[r * (kLatent / 4) + 4 * lane + k] : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < 4; ++k)
+          v[j][k] = ok ? po[(r * 128 + (col0 >> 2) + k) * H + h] : make_float4(0.f, 0.f, 0.f, 0.f);
       }
       float mn = m;
 #pragma unroll
@@ -104,16 +109,16 @@ mla_splitk_reduce_kernel(uint8_t* __restrict__ ws, int U, int H, int slots_cap, 
 #pragma unroll
   for (int k = 0; k < 8; ++k)
     pk[k] = (uint32_t)float_to_bf16_bits_rn(acc[2 * k] * inv) | ((uint32_t)float_to_bf16_bits_rn(acc[2 * k + 1] * inv) << 16);
-  uint4* dst = reinterpret_cast<uint4*>(out + row * kLatent) + 2 * lane;
+  uint4* dst = reinterpret_cast<uint4*>(out + row * kLatent + col0);
   dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
   dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-  if (lse && lane == 0) lse[row] = l > 0.f ? m + logf(l) : -INFINITY;
+  if (lse && blockIdx.z == 0 && warp == 0) lse[row] = l > 0.f ? m + logf(l) : -INFINITY;
 }
 
 cudaError_t launch_splitk_reduce(uint8_t* ws, int U, int H, int slots_cap, int status_ctas, const float* sinks,
                                  uint16_t* out, float* lse, cudaStream_t stream, bool pdl) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(U, (H + kReduceHeads - 1) / kReduceHeads);
+  cfg.gridDim = dim3(U, (H + kReduceHeads - 1) / kReduceHeads, kLatent / (16 * kReduceColGroups));
   cfg.blockDim = dim3(kReduceThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
