@@ -195,6 +195,24 @@ def workload_config(w, l2_note: str, window: int = 0, sinks: bool = False):
     return cfg
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise maximum of `values` over all ranks (the slowest rank's times), or the
+    values themselves with one rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_rate(units_per_rank: float, seconds: float, world: int) -> float:
+    """Whole-job throughput: every rank processes its own copy of the workload (weak
+    scaling), so the job moves world x the per-rank units in the slowest rank's time."""
+    return world * units_per_rank / seconds
+
+
 def dist_setup(n_gpus: int):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -360,10 +378,7 @@ def run_ours(args):
             e2e_ms.append(a.elapsed_time(b))
     e2e_mean = sum(e2e_ms) / len(e2e_ms)
 
-    if world > 1:
-        t = torch.tensor([t_mean, e2e_mean], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_mean, e2e_mean = float(t[0]), float(t[1])
+    t_mean, e2e_mean = max_over_ranks([t_mean, e2e_mean], dev)
     if rank != 0:
         dist.destroy_process_group()
         return
@@ -384,7 +399,7 @@ def run_ours(args):
 
     cpu_kv, cpu_el, cpu_req, cpu_rows = cpu_oracle_sample(inp, args.cpu_seconds, window=args.window, sinks=h_sinks)
     line = {
-        "metric": METRIC, "value": world * kv_bytes / t_s / 1e9, "unit": "GB/s", "n_gpus": world,
+        "metric": METRIC, "value": job_rate(kv_bytes, t_s, world) / 1e9, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_mean, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": workload_config(w, "flushed between steps (512 MB write, then 256 MB read so no dirty lines remain)",
@@ -397,7 +412,7 @@ def run_ours(args):
         "cpu_baseline": {"value": cpu_kv / cpu_el / 1e9, "unit": "GB/s", "cores": cores_used(), "kind": "oracle",
                          "sample": f"{cpu_req} whole requests ({cpu_rows} (b,i) rows x {w.H} heads) of the same "
                                    f"workload, {cpu_el:.1f} s, float64 NumPy"},
-        "e2e": {"value": world * kv_bytes / (e2e_mean * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_rate(kv_bytes, e2e_mean * 1e-3, world) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_mean,
                 "note": "q_nope, q_pe, block_table, seq_lens copied in from pinned host memory and out, lse "
                         "copied back every step; the KV cache is resident device state"},
