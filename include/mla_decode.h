@@ -273,7 +273,7 @@ mla_status_t mla_batched_gemv(const void *x, int64_t x_token_stride, int64_t x_h
  *   - A shape whose workspace (mla_decode_workspace_size) exceeds
  *     MLA_NO_ALLOC_SCRATCH_BYTES returns MLA_ERR_WORKSPACE_TOO_SMALL; nothing is enqueued.
  *   - All calls on a device share the one buffer, which keeps the last call's contents;
- *     each call resets the status word it needs zeroed and overwrites the rest.  Calls
+ *     each call overwrites everything it reads (the status word included).  Calls
  *     that overlap on the GPU (other streams, other host threads) race on the buffer:
  *     the caller must order them.
  *   - *scratch_used (may be NULL) receives the buffer's device address, e.g. for

@@ -56,6 +56,15 @@ mla_batched_gemv_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
   const uint32_t ncols = tmem_cols(tt);
   volatile int* abort_flag = &C.abort;
 
+  const uint32_t smem0 = ptx::smem_u32(smem);
+  auto issue = [&](int kc) {  // K chunk kc of the weight rows and of the token rows
+    const int st = kc % stages;
+    const uint32_t a = smem0 + st * stage_bytes(tt), full = ptx::smem_u32(&C.full[st]);
+    ptx::mbar_arrive_expect_tx(full, stage_bytes(tt));
+    ptx::tma_load_2d(a, &tm_w, kc * kBlockK, h * N + n0, full);
+    ptx::tma_load_3d(a + kABytes, &tm_x, kc * kBlockK, h, t0, full);
+  };
+  const int first = nk < stages ? nk : stages;
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       ptx::mbar_init(ptx::smem_u32(&C.full[s]), 1);
@@ -64,10 +73,10 @@ mla_batched_gemv_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
     ptx::mbar_init(ptx::smem_u32(&C.done), 1);
     C.abort = 0;
     ptx::fence_mbar_init_cluster();
-    ptx::prefetch_tmap(&tm_w);
-    ptx::prefetch_tmap(&tm_x);
+    // the first ring's worth of loads leaves before the TMEM allocation and the block barrier
+    for (int kc = 0; kc < first; ++kc) issue(kc);
   }
-  if (warp == 0) {
+  if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(&C.tmem), ncols);
     ptx::tmem_relinquish();
   }
@@ -75,18 +84,14 @@ mla_batched_gemv_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = C.tmem;
-  const uint32_t smem0 = ptx::smem_u32(smem);
 
   if (warp == 0 && lane == 0) {
-    // ---- producer: K chunks of the weight rows and of the token rows
-    int kc = 0;
+    // ---- producer: the remaining K chunks, each into a stage its MMAs have released
+    int kc = first;
     for (; kc < nk; ++kc) {
       const int st = kc % stages;
-      if (kc >= stages && !ptx::mbar_wait(ptx::smem_u32(&C.empty[st]), ((kc / stages) - 1) & 1, abort_flag)) break;
-      const uint32_t a = smem0 + st * stage_bytes(tt), full = ptx::smem_u32(&C.full[st]);
-      ptx::mbar_arrive_expect_tx(full, stage_bytes(tt));
-      ptx::tma_load_2d(a, &tm_w, kc * kBlockK, h * N + n0, full);
-      ptx::tma_load_3d(a + kABytes, &tm_x, kc * kBlockK, h, t0, full);
+      if (!ptx::mbar_wait(ptx::smem_u32(&C.empty[st]), ((kc / stages) - 1) & 1, abort_flag)) break;
+      issue(kc);
     }
     // loads still in flight after an abort land before the CTA exits
     for (int k = max(0, kc - stages); k < kc; ++k)
@@ -137,7 +142,7 @@ mla_batched_gemv_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
   }
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 0) ptx::tmem_dealloc(tmem, ncols);
+  if (warp == 1) ptx::tmem_dealloc(tmem, ncols);
 }
 
 }  // namespace gemv

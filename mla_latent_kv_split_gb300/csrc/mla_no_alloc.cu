@@ -51,8 +51,8 @@ MLA_EXPORT mla_status_t mla_decode_no_alloc(const void* q_nope, const void* q_pe
   st = scratch_on_current_device(&scratch);
   if (st != MLA_OK) return st;
   if (scratch_used) *scratch_used = scratch;
-  // mla_decode resets the status word at the start of the scratch; the plan and the
-  // partials need no initialisation and are overwritten by each call.
+  // every word of the scratch a call reads (status words, plan, partials) is written
+  // earlier in the same call: the buffer needs no initialisation
   return mla_decode(q_nope, q_pe, kv_cache, block_table, max_pages, seq_lens, B, q_len, H, num_pages, page_size,
                     sm_scale, kv_dtype, kv_scale, num_splits, scratch, (size_t)MLA_NO_ALLOC_SCRATCH_BYTES, out,
                     lse, stream);
