@@ -32,9 +32,10 @@ constexpr int kNvfp4Group = 16;
 //   [kPlanOffset, +8*units)     plan: per unit {parts, first partial slot}
 //   [kCtaStatusOffset, +4*CTAs) status bits of each decode CTA (written unconditionally at its
 //                               exit; the split-K reduce ORs them into the status word)
-//   [kHeaderBytes, ...)         partial outputs  fp32 [slots][128][H][4]: column quads
+//   [kHeaderBytes, ...)         partial outputs  bf16 [slots][64][H][8]: column octets
 //                               outermost, so that 32 consecutive heads' values of one
-//                               quad are 512 contiguous bytes
+//                               octet are 512 contiguous bytes (the region is sized for
+//                               fp32, slots*H*512*4 bytes, of which half is used)
 //   then                        partial LSEs     fp32 [slots][H]
 constexpr size_t kPlanOffset = 256;
 constexpr size_t kCtaStatusOffset = 16384;

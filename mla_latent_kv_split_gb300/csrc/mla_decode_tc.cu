@@ -947,9 +947,10 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       const bool direct = it.slot < 0, partial = it.slot >= 0 && it.slot < p.slots_cap;
       // A final output leaves through shared memory and TMA tensor stores (16 columns x 16
       // rows per box): a thread's row is not contiguous with its neighbours' in [U, H, 512].
-      // A split partial is stored straight from registers: in the workspace's quad-major
-      // layout a warp's 32 rows of one column quad are 512 contiguous bytes, so the stores
-      // need no staging and the next item's P.V can start as soon as O has been read.
+      // A split partial is stored straight from registers, as bf16: in the workspace's
+      // octet-major layout a warp's 32 rows of one 8-column octet are 512 contiguous bytes,
+      // so the stores need no staging and the next item's P.V can start as soon as O has
+      // been read.
       const int row0 = it.u * p.H + 32 * q;
       // The worker's last item (the ring's next entry is the end marker): the cache stages
       // are idle, so each chunk gets a staging buffer of its own there and all stores are in
@@ -961,8 +962,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       }
       last = __all_sync(0xffffffffu, last);
       uint8_t* const stg0 = last ? S.stage[0] + sw * 16384 : S.ostage[sw];
-      float* const part =
-          reinterpret_cast<float*>(p.ws + partial_o_offset()) + ((size_t)it.slot * 128 * p.H + row) * 4;
+      uint4* const part = reinterpret_cast<uint4*>(p.ws + partial_o_offset()) + (size_t)it.slot * 64 * p.H + row;
       const uint64_t pol_keep = ptx::l2_policy_evict_last();  // read again by the combine
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
@@ -971,12 +971,16 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
         ptx::tmem_ld_wait();
         if (!direct) {
           if (partial && real) {
-            const int quad0 = (256 * (int)cr + 128 * wg + 16 * c) >> 2;
+            const int oct0 = (256 * (int)cr + 128 * wg + 16 * c) >> 3;
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              ptx::st_global_v4_hint(part + (size_t)(quad0 + k) * p.H * 4, __uint_as_float(r[4 * k]) * oscale,
-                                     __uint_as_float(r[4 * k + 1]) * oscale, __uint_as_float(r[4 * k + 2]) * oscale,
-                                     __uint_as_float(r[4 * k + 3]) * oscale, pol_keep);
+            for (int k = 0; k < 2; ++k)
+              ptx::st_global_v4u_hint(
+                  part + (size_t)(oct0 + k) * p.H,
+                  make_uint4(ptx::pack_bf16x2(__uint_as_float(r[8 * k]) * oscale, __uint_as_float(r[8 * k + 1]) * oscale),
+                             ptx::pack_bf16x2(__uint_as_float(r[8 * k + 2]) * oscale, __uint_as_float(r[8 * k + 3]) * oscale),
+                             ptx::pack_bf16x2(__uint_as_float(r[8 * k + 4]) * oscale, __uint_as_float(r[8 * k + 5]) * oscale),
+                             ptx::pack_bf16x2(__uint_as_float(r[8 * k + 6]) * oscale, __uint_as_float(r[8 * k + 7]) * oscale)),
+                  pol_keep);
           }
           continue;
         }

@@ -196,6 +196,11 @@ __device__ __forceinline__ void st_global_v4_hint(void* ptr, float a, float b, f
                ::"l"(ptr), "f"(a), "f"(b), "f"(c), "f"(d), "l"(policy)
                : "memory");
 }
+__device__ __forceinline__ void st_global_v4u_hint(void* ptr, uint4 v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;"
+               ::"l"(ptr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(policy)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Every committed bulk store of this thread has read its shared-memory source.
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }

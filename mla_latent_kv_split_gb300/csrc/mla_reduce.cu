@@ -12,8 +12,8 @@
 // status bits into the call's status word.
 //
 // One CTA of 256 threads per (unit, 32 heads, 128 columns): lane = head, warp = one 16-column
-// group.  The partials are stored column-quad-major ([slot][128][H][4] fp32), so for one
-// quad a warp's 32 heads are 512 contiguous bytes; each thread reads its 16 columns as four
+// group.  The partials are stored column-octet-major ([slot][64][H][8] bf16), so for one
+// octet a warp's 32 heads are 512 contiguous bytes; each thread reads its 16 columns as two
 // such coalesced loads per part and writes its 32 output bytes whole.  Every load of a
 // group of parts is issued before any is used: a part group costs one memory round trip,
 // and the whole grid (units x H/32 x 4 CTAs) is resident at once.
@@ -28,7 +28,7 @@ namespace mla {
 constexpr int kReduceThreads = 256;
 constexpr int kReduceHeads = 32;                     // lanes
 constexpr int kReduceColGroups = kReduceThreads / 32;  // warps: 16 columns each
-constexpr int kPartGroup = 2;
+constexpr int kPartGroup = 3;
 
 __global__ void __launch_bounds__(kReduceThreads, 4)
 mla_splitk_reduce_kernel(uint8_t* __restrict__ ws, int U, int H, int slots_cap, int status_ctas,
@@ -57,18 +57,17 @@ mla_splitk_reduce_kernel(uint8_t* __restrict__ ws, int U, int H, int slots_cap, 
   float m = -INFINITY, l = 0.f;
   if (parts > 1 && slot >= 0 && slot + parts <= slots_cap) {
     const float* pls = reinterpret_cast<const float*>(ws + partial_lse_offset(slots_cap, H));
-    const float4* po = reinterpret_cast<const float4*>(ws + partial_o_offset());
+    const uint4* po = reinterpret_cast<const uint4*>(ws + partial_o_offset());
     for (int s0 = 0; s0 < parts; s0 += kPartGroup) {
       float ls[kPartGroup];
-      float4 v[kPartGroup][4];
+      uint4 v[kPartGroup][2];
 #pragma unroll
       for (int j = 0; j < kPartGroup; ++j) {
         const bool ok = s0 + j < parts;
         const size_t r = (size_t)(slot + s0 + j);
         ls[j] = ok ? pls[r * H + h] : -INFINITY;
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          v[j][k] = ok ? po[(r * 128 + (col0 >> 2) + k) * H + h] : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < 2; ++k) v[j][k] = ok ? po[(r * 64 + (col0 >> 3) + k) * H + h] : make_uint4(0u, 0u, 0u, 0u);
       }
       float mn = m;
 #pragma unroll
@@ -83,11 +82,13 @@ mla_splitk_reduce_kernel(uint8_t* __restrict__ ws, int U, int H, int slots_cap, 
         const float w = expf(ls[j] - mn);  // missing parts: -inf -> 0
         l += w;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          acc[4 * k] = fmaf(w, v[j][k].x, acc[4 * k]);
-          acc[4 * k + 1] = fmaf(w, v[j][k].y, acc[4 * k + 1]);
-          acc[4 * k + 2] = fmaf(w, v[j][k].z, acc[4 * k + 2]);
-          acc[4 * k + 3] = fmaf(w, v[j][k].w, acc[4 * k + 3]);
+        for (int k = 0; k < 2; ++k) {
+          const uint32_t e[4] = {v[j][k].x, v[j][k].y, v[j][k].z, v[j][k].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            acc[8 * k + 2 * i] = fmaf(w, __uint_as_float(e[i] << 16), acc[8 * k + 2 * i]);
+            acc[8 * k + 2 * i + 1] = fmaf(w, __uint_as_float(e[i] & 0xFFFF0000u), acc[8 * k + 2 * i + 1]);
+          }
         }
       }
       m = mn;

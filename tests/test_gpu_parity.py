@@ -68,9 +68,9 @@ def test_forced_splits_and_partials(n):
         lambda b, i, nv: oracle.forced_split_ranges(nv, n), page_size=64)
     wsn = ws.cpu().numpy()
     slots_cap = (wsn.size - 32768) // (w.H * 513 * 4)
-    # partial outputs are stored column-quad-major: [slot][128 quads][H][4]
-    po = wsn[32768:32768 + slots_cap * w.H * 512 * 4].view(np.float32).reshape(slots_cap, 128, w.H, 4)
-    po = po.transpose(0, 2, 1, 3).reshape(slots_cap, w.H, 512)
+    # partial outputs are bf16, stored column-octet-major: [slot][64 octets][H][8]
+    bits = wsn[32768:32768 + slots_cap * w.H * 512 * 2].view(np.uint16).reshape(slots_cap, 64, w.H, 8)
+    po = oracle.decode_bf16(bits.transpose(0, 2, 1, 3).reshape(slots_cap, w.H, 512))
     pls = wsn[32768 + slots_cap * w.H * 512 * 4:][: slots_cap * w.H * 4].view(np.float32).reshape(slots_cap, w.H)
     for b in range(2):
         if pl["parts"][b] > 1:
