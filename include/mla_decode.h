@@ -114,7 +114,9 @@ mla_status_t mla_decode_workspace_size(int B, int q_len, int H, int num_splits, 
  *               ignored for the other formats.  The FP8 scale multiplies every stored
  *               value, so it applies to both the scores and the output.
  *   num_splits  0: the library picks the split of every request from the SM count and
- *               all seq_lens (read on the device); > 0: every request is cut into at
+ *               all seq_lens (read on the device): the tiles of all (b, i), each preceded
+ *               by a fixed per-item cost, are cut into equal contiguous ranges, one per
+ *               pair of SMs; > 0: every request is cut into at
  *               most num_splits ranges of roundup(cdiv(len, num_splits), 64) tokens.
  *   workspace   device scratch of workspace_bytes >= mla_decode_workspace_size(...);
  *               its contents need no initialisation and are overwritten.
@@ -187,7 +189,9 @@ mla_status_t mla_decode_num_workers(int *workers);
 
 /*
  * Host copy of the device schedule, for tests: for the given seq_lens (HOST array), fills
- * per (b, i) unit: first tile, tile count, number of parts and first partial slot
+ * per (b, i) unit: its first position in the schedule (num_splits == 0: the first of its
+ * 4 + tiles balancing slots, 4 standing for the fixed cost of a work item; num_splits > 0:
+ * its first item), tile count, number of parts and first partial slot
  * (-1 when the unit is written directly); returns the number of partial slots used.
  * Arrays have B*q_len entries.  `window` as in mla_decode_ex (tile counts then start at
  * the window's first tile).  `workers` <= 0 means the current device's worker count.

@@ -73,9 +73,15 @@ MLA_HD int window_first(int vis, int window) { return window > 0 && vis > window
 MLA_HD int unit_tile0(int vis, int window) { return window_first(vis, window) / kTile; }
 MLA_HD int unit_tiles(int vis, int window) { return vis > 0 ? cdiv_i(vis, kTile) - unit_tile0(vis, window) : 0; }
 
-// ---- heuristic mode (num_splits == 0): contiguous, balanced tile ranges per worker ----
-// With N tiles and C workers, only C' = min(C, N) workers get work, so no range is empty;
-// worker c < C' owns global tiles [floor(c*N/C'), floor((c+1)*N/C')).  Callers pass C'.
+// ---- heuristic mode (num_splits == 0): contiguous, balanced ranges per worker ----
+// Every unit with visible KV is laid out as kItemCost placeholder slots (the fixed cost of
+// starting a work item on it: its query load, pipeline refill and epilogue, measured at
+// about four tiles' time) followed by its tiles.  With N slots in all and C workers, only
+// C' = min(C, N) workers get a range, worker c < C' owning slots [floor(c*N/C'),
+// floor((c+1)*N/C')); its work is the tiles inside that range.  A worker that starts a new
+// unit inside its range thereby gets fewer tiles.  Callers pass C'.
+constexpr int kItemCost = 4;
+MLA_HD int unit_slots(int tiles) { return tiles > 0 ? tiles + kItemCost : 0; }
 MLA_HD int active_workers(long long N, int C) { return N < (long long)C ? (int)N : C; }
 MLA_HD long long worker_begin(int c, long long N, int C) { return (long long)c * N / C; }
 // The worker whose range holds tile t (0 <= t < N): the largest c with begin(c) <= t.
@@ -115,8 +121,8 @@ inline int plan_host(const int32_t* seq_lens, int B, int q_len, int max_pages, i
       plan[u].tile_begin = (int)N;  // first item index
       N += plan[u].parts;
     } else {
-      plan[u].tile_begin = (int)N;
-      N += plan[u].tiles;
+      plan[u].tile_begin = (int)N;  // first slot (its tiles start kItemCost slots later)
+      N += unit_slots(plan[u].tiles);
     }
   }
   int slots = 0;
@@ -126,8 +132,9 @@ inline int plan_host(const int32_t* seq_lens, int B, int q_len, int max_pages, i
       if (plan[u].tiles == 0) {
         plan[u].parts = 0;
       } else {
-        int c0 = worker_of(plan[u].tile_begin, N, Ca);
-        int c1 = worker_of((long long)plan[u].tile_begin + plan[u].tiles - 1, N, Ca);
+        const long long r0 = (long long)plan[u].tile_begin + kItemCost;
+        int c0 = worker_of(r0, N, Ca);
+        int c1 = worker_of(r0 + plan[u].tiles - 1, N, Ca);
         plan[u].parts = c1 - c0 + 1;
       }
     }

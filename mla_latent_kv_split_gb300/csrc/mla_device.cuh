@@ -139,7 +139,7 @@ __device__ inline void compute_plan(const DecodeParams& p, PlanSmem& pl, int* sc
     int tiles = unit_tiles(vis, p.window);
     pl.begin[u] = p.num_splits > 0
                       ? (tiles ? cdiv_i(tiles, forced_span_tiles(tiles, p.num_splits)) : 0)
-                      : tiles;
+                      : unit_slots(tiles);
   }
   if (bad && write_plan) set_status(cta_status, bad);
   __syncthreads();
@@ -156,9 +156,10 @@ __device__ inline void compute_plan(const DecodeParams& p, PlanSmem& pl, int* sc
     if (p.num_splits > 0) {
       parts = pl.begin[u + 1] - pl.begin[u];
     } else {
-      int tiles = pl.begin[u + 1] - pl.begin[u];
-      parts = tiles ? worker_of(pl.begin[u + 1] - 1, N, Ca) - worker_of(pl.begin[u], N, Ca) + 1
-                    : 0;
+      // a unit's tiles are the last of its slots
+      parts = pl.begin[u + 1] > pl.begin[u]
+                  ? worker_of(pl.begin[u + 1] - 1, N, Ca) - worker_of(pl.begin[u] + kItemCost, N, Ca) + 1
+                  : 0;
     }
     pl.slot[u] = parts > 1 ? parts : 0;
     if (write_plan) {
@@ -172,7 +173,7 @@ __device__ inline void compute_plan(const DecodeParams& p, PlanSmem& pl, int* sc
   for (int u = tid; u < U; u += T) {
     int parts = p.num_splits > 0 ? pl.begin[u + 1] - pl.begin[u]
               : (pl.begin[u + 1] > pl.begin[u]
-                     ? worker_of(pl.begin[u + 1] - 1, N, Ca) - worker_of(pl.begin[u], N, Ca) + 1
+                     ? worker_of(pl.begin[u + 1] - 1, N, Ca) - worker_of(pl.begin[u] + kItemCost, N, Ca) + 1
                      : 0);
     if (parts <= 1) pl.slot[u] = -1;
     if (write_plan) {
@@ -238,12 +239,16 @@ __device__ inline WorkerStart worker_start(const DecodeParams& p, const PlanSmem
     const int span = forced_span_tiles(tiles, p.num_splits);
     const int lo = k * span, hi = min((k + 1) * span, tiles);
     w.first = WorkItem{u, (t0 + lo) * kTile, min((t0 + hi) * kTile, vis), pl.slot[u] >= 0 ? pl.slot[u] + k : -1, tmin};
-  } else {  // tiles [first, end of the worker's range or of the unit)
+  } else {  // the unit's tiles inside [first, end of the worker's range)
     const long long e = worker_begin(c + 1, pl.N, Ca);
-    const int lo = first - w.base0;
-    const int hi = (int)(min(e, (long long)w.base0 + tiles) - w.base0);
-    w.first = WorkItem{u, (t0 + lo) * kTile, min((t0 + hi) * kTile, vis),
-                       pl.slot[u] >= 0 ? pl.slot[u] + (c - worker_of(w.base0, pl.N, Ca)) : -1, tmin};
+    const long long r0 = (long long)w.base0 + kItemCost;  // the unit's first tile
+    const long long lo = max((long long)first, r0), hi = min(e, r0 + tiles);
+    if (hi <= lo) {  // the range ends inside the unit's placeholder slots: no work
+      w.busy = 0;
+      return w;
+    }
+    w.first = WorkItem{u, (t0 + (int)(lo - r0)) * kTile, min((t0 + (int)(hi - r0)) * kTile, vis),
+                       pl.slot[u] >= 0 ? pl.slot[u] + (c - worker_of(r0, pl.N, Ca)) : -1, tmin};
   }
   return w;
 }
@@ -312,16 +317,17 @@ __device__ inline bool next_item(const DecodeParams& p, int N, ItemCursor& k, Wo
   while (k.t < k.e) {
     const int vis = unit_visible_dev(p, k.u);
     const int tiles = unit_tiles(vis, p.window);
-    const long long te = k.tb + tiles;
-    const int parts = tiles ? worker_of(te - 1, N, Ca) - worker_of(k.tb, N, Ca) + 1 : 0;
-    const bool emit = te > k.t;
+    const long long te = k.tb + unit_slots(tiles);  // the unit's slots end
+    const long long r0 = k.tb + kItemCost;          // its first tile
+    const int parts = tiles ? worker_of(te - 1, N, Ca) - worker_of(r0, N, Ca) + 1 : 0;
+    const long long lo = max(k.t, r0), hi = min(k.e, te);
+    const bool emit = tiles > 0 && hi > lo;
     if (emit) {
-      const int lo = (int)(k.t - k.tb), hi = (int)(min(k.e, te) - k.tb);
       const int t0 = unit_tile0(vis, p.window);
-      it = WorkItem{k.u, (t0 + lo) * kTile, min((t0 + hi) * kTile, vis),
-                    parts > 1 ? k.sacc + (k.c - worker_of(k.tb, N, Ca)) : -1, window_first(vis, p.window)};
-      k.t = min(k.e, te);
+      it = WorkItem{k.u, (t0 + (int)(lo - r0)) * kTile, min((t0 + (int)(hi - r0)) * kTile, vis),
+                    parts > 1 ? k.sacc + (k.c - worker_of(r0, N, Ca)) : -1, window_first(vis, p.window)};
     }
+    k.t = max(k.t, min(k.e, te));
     if (k.t >= te) {
       k.sacc += parts > 1 ? parts : 0;
       k.tb = te;

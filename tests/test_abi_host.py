@@ -12,6 +12,7 @@ import oracle
 from mla_latent_kv_split_gb300 import binding as mb
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+ITEM_COST = 4  # placeholder slots per work item in the library's balanced split
 
 
 @pytest.fixture(scope="module")
@@ -100,8 +101,11 @@ def _check_plan(seq_lens, q_len, ps, num_splits, C, max_pages=None, window=0):
                 assert pl["parts"][u] == -(-int(tiles[u]) // span) <= num_splits
     else:
         assert used <= 2 * C
-        # brute force: assign tiles to workers by the balanced rule and count parts
-        N = int(tiles.sum())
+        # brute force: every unit with tiles is ITEM_COST placeholder slots then its tiles;
+        # the slots are dealt to workers by the balanced rule and a unit's parts are the
+        # workers holding any of its tiles
+        slots_u = np.where(tiles > 0, tiles + ITEM_COST, 0)
+        N = int(slots_u.sum())
         Ca = min(C, N)
         owner = np.empty(N, dtype=np.int64)
         for c in range(Ca):
@@ -109,9 +113,11 @@ def _check_plan(seq_lens, q_len, ps, num_splits, C, max_pages=None, window=0):
         t0 = 0
         for u in range(U):
             if tiles[u]:
-                assert pl["parts"][u] == len(set(owner[t0:t0 + tiles[u]].tolist()))
-            t0 += tiles[u]
-        # balance: every active worker gets floor or ceil of N / Ca tiles
+                assert pl["tile_begin"][u] == t0
+                real = owner[t0 + ITEM_COST:t0 + ITEM_COST + tiles[u]]
+                assert pl["parts"][u] == len(set(real.tolist()))
+            t0 += slots_u[u]
+        # balance: every active worker gets floor or ceil of N / Ca slots
         if N:
             counts = np.bincount(owner, minlength=Ca)
             assert counts.max() - counts.min() <= 1
