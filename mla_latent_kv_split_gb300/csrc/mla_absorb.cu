@@ -20,6 +20,7 @@
 
 #include "../../include/mla_decode.h"
 #include "mla_ptx.cuh"
+#include "mla_tmap.cuh"
 
 namespace mla {
 namespace gemv {
@@ -147,25 +148,6 @@ mla_batched_gemv_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
 
 }  // namespace gemv
 
-namespace {
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-EncodeTiledFn gemv_encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-  }
-  return fn;
-}
-}  // namespace
-
 // Token tile: at most 256 tokens per CTA, tiles balanced, rounded up to 16 (MMA N).
 int gemv_token_tile(int T) {
   const int tiles = (T + gemv::kMaxTokens - 1) / gemv::kMaxTokens;
@@ -177,7 +159,7 @@ cudaError_t launch_batched_gemv(const uint16_t* x, long long x_token_stride, lon
                                 const uint16_t* w, uint16_t* out, long long out_token_stride,
                                 long long out_head_stride, int T, int H, int N, int K, uint32_t* status,
                                 cudaStream_t stream) {
-  EncodeTiledFn fn = gemv_encode_fn();
+  EncodeTiledFn fn = tmap_encode_fn();
   if (!fn) return cudaErrorNotSupported;
   const int tt = gemv_token_tile(T);
   const int nk = (K + gemv::kBlockK - 1) / gemv::kBlockK;

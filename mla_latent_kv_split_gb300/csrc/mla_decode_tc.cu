@@ -53,6 +53,7 @@
 
 #include "mla_device.cuh"
 #include "mla_ptx.cuh"
+#include "mla_tmap.cuh"
 
 namespace mla {
 namespace tc {
@@ -1067,29 +1068,12 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
 
 // ---------------------------------------------------------------------- host side
 namespace {
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-  }
-  return fn;
-}
 
 // 2-D view of a bf16 or FP8 cache: [num_pages * page_size rows, 576 columns], one page of
 // rows per box.
 bool encode_cache_map(CUtensorMap* m, const void* cache, int num_pages, int ps, int box_cols, int elem_bytes,
                       CUtensorMapSwizzle sw) {
-  EncodeTiledFn fn = encode_fn();
+  EncodeTiledFn fn = tmap_encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)kDim, (cuuint64_t)num_pages * ps};
   cuuint64_t strides[1] = {(cuuint64_t)kDim * elem_bytes};
@@ -1101,7 +1085,7 @@ bool encode_cache_map(CUtensorMap* m, const void* cache, int num_pages, int ps, 
 }
 // Row-major [rows, 512] output tensor (bf16 or fp32), boxes of 16 columns x 16 rows.
 bool encode_rows_map(CUtensorMap* m, const void* base, size_t rows, int elem_bytes, CUtensorMapSwizzle sw) {
-  EncodeTiledFn fn = encode_fn();
+  EncodeTiledFn fn = tmap_encode_fn();
   if (!fn || rows == 0) return false;
   cuuint64_t dims[2] = {(cuuint64_t)kLatent, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)kLatent * elem_bytes};
