@@ -18,6 +18,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/mla_decode.h"
 #include "mla_ptx.cuh"
 #include "mla_tmap.cuh"
@@ -30,6 +32,7 @@ constexpr int kBlockM = 128;     // weight rows per CTA
 constexpr int kBlockK = 64;      // bf16 columns per K chunk: one 128-byte swizzle row
 constexpr int kMaxStages = 8;
 constexpr uint32_t kStageBudget = 200 * 1024;  // shared memory for the stage ring
+constexpr uint32_t kMaxSmem = kStageBudget + 8 * 1024;  // ring + control words + alignment, at most
 constexpr int kMaxTokens = 256;  // tokens per CTA (MMA N)
 constexpr uint32_t kABytes = kBlockM * kBlockK * 2;
 
@@ -195,9 +198,24 @@ cudaError_t launch_batched_gemv(const uint16_t* x, long long x_token_stride, lon
   const size_t sm_smem = 233472;  // per-SM shared memory (228 KB)
   const size_t floor_smem = sm_smem / (512 / cols + 1) + 1;
   if (smem < floor_smem) smem = floor_smem;
+  if (smem > gemv::kMaxSmem) return cudaErrorInvalidValue;  // cannot happen: the ring fits kStageBudget
   auto kern = gemv::mla_batched_gemv_kernel;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  // the opt-in (the largest ring this launcher ever asks for) outlives the call: set once
+  // per device
+  static std::mutex mu;
+  static bool opted_in[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (!opted_in[dev]) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gemv::kMaxSmem);
+      if (e != cudaSuccess) return e;
+      opted_in[dev] = true;
+    }
+  }
   dim3 grid((N + gemv::kBlockM - 1) / gemv::kBlockM, H, (T + tt - 1) / tt);
   kern<<<grid, gemv::kThreads, smem, stream>>>(tm_w, tm_x, out, out_token_stride, out_head_stride, T, N, K, tt, stages,
                                                status);

@@ -51,6 +51,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "mla_device.cuh"
 #include "mla_ptx.cuh"
 #include "mla_tmap.cuh"
@@ -1133,8 +1135,21 @@ template <int KV>
 static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o, const DecodeParams& p,
                              cudaStream_t stream) {
   auto kern = tc::mla_decode_tc_kernel<KV>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem_bytes());
+  // the shared-memory opt-in outlives the call: set once per device
+  static std::mutex mu;
+  static bool opted_in[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (!opted_in[dev]) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem_bytes());
+      if (e != cudaSuccess) return e;
+      opted_in[dev] = true;
+    }
+  }
   kern<<<2 * p.workers, tc::kThreads, tc_smem_bytes(), stream>>>(a, b, o, p);
   return cudaGetLastError();
 }
