@@ -139,10 +139,11 @@ struct Bars {
                                // bf16: masked rows zeroed by the producer warp, those tiles only)
   uint64_t kv_empty[kStages];  // P.V of the tile completed: stage reusable
   uint64_t s_full[2];          // S MMAs of a buffer completed
-  uint64_t s_free[2];          // the senders and the buffer's softmax warpgroup read its S
+  uint64_t s_free[2];          // the buffer's softmax warpgroup (and the senders, when they send) read its S
   uint64_t p_full[2];          // P written to the exchange slot (and O rescaled)
   uint64_t o_done[4];          // P.V of tile g completed (barrier g & 3)
   uint64_t q_ready;            // Q of the next item in TMEM / shared memory
+  uint64_t q_free;             // every score MMA of an item completed: its Q may be replaced
   uint64_t o_free;             // epilogue read O
   uint64_t x_full[2];          // the peer's partial scores landed in my exchange slot (tx count)
   uint64_t x_empty[2];         // the peer's P.V read its slot: I may push the next scores into it
@@ -342,6 +343,12 @@ template <int KV>
 constexpr bool decode_in_softmax() { return KV == MLA_KV_NVFP4; }
 template <int KV>
 constexpr bool decode_in_senders() { return KV == MLA_KV_FP8_E4M3; }
+// Who pushes a tile's partial scores to the peer CTA.  FP8: the tile's softmax warpgroup,
+// straight from the scores it has just read, so that the senders, which decode every tile,
+// never hold a send back behind a tile still in flight (A/B on one box: 472 -> 417 us on the
+// FP8 workload).  bf16 / NVFP4: the senders, which otherwise only load Q (3-4 % faster there).
+template <int KV>
+constexpr bool send_in_softmax() { return KV == MLA_KV_FP8_E4M3; }
 
 // KV: cache format (MLA_KV_BF16 / MLA_KV_FP8_E4M3 / MLA_KV_NVFP4).  The MMAs run in bf16 for a
 // bf16 cache and in f16 for the quantized ones (E4M3 and E2M1 x E4M3 are exact in f16).
@@ -377,6 +384,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
   const uint32_t b_s_full = ptx::smem_u32(&S.bars.s_full[0]), b_s_free = ptx::smem_u32(&S.bars.s_free[0]);
   const uint32_t b_p_full = ptx::smem_u32(&S.bars.p_full[0]), b_o_done = ptx::smem_u32(&S.bars.o_done[0]);
   const uint32_t b_q_ready = ptx::smem_u32(&S.bars.q_ready), b_o_free = ptx::smem_u32(&S.bars.o_free);
+  const uint32_t b_q_free = ptx::smem_u32(&S.bars.q_free);
   const uint32_t b_x_full = ptx::smem_u32(&S.bars.x_full[0]), b_x_empty = ptx::smem_u32(&S.bars.x_empty[0]);
   const uint32_t b_mma_final = ptx::smem_u32(&S.bars.mma_final);
   const uint32_t b_mma_final_pv = ptx::smem_u32(&S.bars.mma_final_pv);
@@ -391,13 +399,14 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
     }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(b_s_full + 8 * s, 1);
-      ptx::mbar_init(b_s_free + 8 * s, kWgThreads + kSenderThreads);
+      ptx::mbar_init(b_s_free + 8 * s, kWgThreads + (send_in_softmax<KV>() ? 0 : kSenderThreads));
       ptx::mbar_init(b_p_full + 8 * s, kWgThreads);
       ptx::mbar_init(b_x_full + 8 * s, 1);   // one local arrive (expect_tx) + 24 KB of peer bytes
       ptx::mbar_init(b_x_empty + 8 * s, 1);  // one arrive per use, from the peer's P.V commit
     }
     for (int s = 0; s < 4; ++s) ptx::mbar_init(b_o_done + 8 * s, 1);
     ptx::mbar_init(b_q_ready, kSenderThreads);
+    ptx::mbar_init(b_q_free, 1);  // one commit per item, after its last score MMAs
     ptx::mbar_init(b_o_free, kSoftmaxThreads);
     ptx::mbar_init(b_ep, kSoftmaxThreads);
     ptx::mbar_init(b_mma_final, 1);
@@ -563,6 +572,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
             ptx::mma_ss(d_s, qdesc0 + (uint64_t)(k * 2), rdesc + (uint64_t)(k * 2), idesc_s, 1u);
           ptx::mma_commit(b_s_full + 8 * (g & 1));
         }
+        if (!dead) ptx::mma_commit(b_q_free);
         ++n_item;
       }
       ptx::mma_commit(b_mma_final);
@@ -697,42 +707,79 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       ptx::tc_fence_before();
       ptx::mbar_arrive(b_q_ready);
     };
-    // Per tile g: when the senders decode (FP8), tile g is decoded first (its score MMAs wait
-    // for it), then tile g-1's scores are sent.  An item's Q is loaded once the previous
-    // item's last scores have been read out of TMEM.
-    int g = 0;
-    bool dead = false;
-    WorkItem it;
-    const int tq = (warp - kWarpSender0) * 32 + lane;
-    // the first item's unit is known from the schedule: its Q loads overlap the item ring's
-    // start and the first cache loads
-    if (wst.busy) load_q(WorkItem{wst.u0, 0, 0, -1, 0});
-    for (int k_item = 0; !dead; ++k_item) {
-      const int got = item_take(S.items, S.items_min, b_item_full, b_item_empty, k_item, abort_flag, it, true);
-      if (got <= 0) {
-        dead = got < 0;
-        break;
+    if constexpr (send_in_softmax<KV>()) {
+      // Per item: its Q once every score MMA of the previous item has completed (they read Q
+      // from TMEM; the score issuer commits one q_free phase per item), then, for FP8, each of
+      // its tiles decoded as soon as it lands.
+      int g = 0;
+      bool dead = false;
+      WorkItem it;
+      const int tq = (warp - kWarpSender0) * 32 + lane;
+      // the first item's unit is known from the schedule: its Q loads overlap the item ring's
+      // start and the first cache loads
+      if (wst.busy) load_q(WorkItem{wst.u0, 0, 0, -1, 0});
+      for (int k_item = 0; !dead; ++k_item) {
+        const int got = item_take(S.items, S.items_min, b_item_full, b_item_empty, k_item, abort_flag, it, true);
+        if (got <= 0) {
+          dead = got < 0;
+          break;
+        }
+        const int nt = (it.tok_hi - it.tok_lo + kTileN - 1) / kTileN;
+        if (k_item > 0) {  // the previous item's score MMAs have all completed (one phase per item)
+          if (!ptx::mbar_wait(b_q_free, (uint32_t)(k_item - 1) & 1u, abort_flag)) {
+            dead = true;
+            break;
+          }
+          ptx::tc_fence_after();
+          load_q(it);
+        }
+        if (decode_in_senders<KV>()) {
+          for (int t = 0; t < nt; ++t)
+            if (!prepare_tile<KV>(S, p, g + t, tq, cr, b_kv_full, b_kv_ready, 3, abort_flag)) {
+              dead = true;
+              break;
+            }
+        }
+        g += nt;
       }
-      for (int t0 = it.tok_lo; t0 < it.tok_hi; t0 += kTileN, ++g) {
-        if (*abort_flag) {
-          dead = true;
+    } else {
+      // Per tile g: tile g-1's scores are sent (the decode step is skipped: these formats are
+      // not decoded by the senders).  An item's Q is loaded once the previous item's last
+      // scores have been read out of TMEM.
+      int g = 0;
+      bool dead = false;
+      WorkItem it;
+      const int tq = (warp - kWarpSender0) * 32 + lane;
+      // the first item's unit is known from the schedule: its Q loads overlap the item ring's
+      // start and the first cache loads
+      if (wst.busy) load_q(WorkItem{wst.u0, 0, 0, -1, 0});
+      for (int k_item = 0; !dead; ++k_item) {
+        const int got = item_take(S.items, S.items_min, b_item_full, b_item_empty, k_item, abort_flag, it, true);
+        if (got <= 0) {
+          dead = got < 0;
           break;
         }
-        if (decode_in_senders<KV>() && !prepare_tile<KV>(S, p, g, tq, cr, b_kv_full, b_kv_ready, 3, abort_flag)) {
-          dead = true;
-          break;
+        for (int t0 = it.tok_lo; t0 < it.tok_hi; t0 += kTileN, ++g) {
+          if (*abort_flag) {
+            dead = true;
+            break;
+          }
+          if (decode_in_senders<KV>() && !prepare_tile<KV>(S, p, g, tq, cr, b_kv_full, b_kv_ready, 3, abort_flag)) {
+            dead = true;
+            break;
+          }
+          if (g > 0 && !send(g - 1)) {
+            dead = true;
+            break;
+          }
+          if (t0 == it.tok_lo && g > 0) load_q(it);
         }
-        if (g > 0 && !send(g - 1)) {
-          dead = true;
-          break;
-        }
-        if (t0 == it.tok_lo && g > 0) load_q(it);
       }
-    }
-    if (!dead && g > 0 && send(g - 1)) {
-      // the peer's last two P.V commits land on this CTA's x_empty: take them before exit
-      for (int k = max(0, g - 2); k < g; ++k)
-        if (!ptx::mbar_wait(b_x_empty + 8 * (k & 1), (k >> 1) & 1, abort_flag, true)) break;
+      if (!dead && g > 0 && send(g - 1)) {
+        // the peer's last two P.V commits land on this CTA's x_empty: take them before exit
+        for (int k = max(0, g - 2); k < g; ++k)
+          if (!ptx::mbar_wait(b_x_empty + 8 * (k & 1), (k >> 1) & 1, abort_flag, true)) break;
+      }
     }
   } else if (warp >= kWarpSoftmax0) {
     // ------------------------------------------------------------------ softmax + epilogue
@@ -747,6 +794,10 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
     const float scale_log2 = p.sm_scale * p.kv_scale * kLog2e;
     const uint32_t b_pf = b_p_full + 8 * wg, b_xf = b_x_full + 8 * wg, b_sf = b_s_full + 8 * wg;
     const uint32_t b_sfree = b_s_free + 8 * wg;
+    // this warpgroup sends its tiles' partial scores into the peer's slot wg
+    const uint32_t x_peer = ptx::mapa(ptx::smem_u32(&S.xbuf[wg][0][0]), peer) + (uint32_t)row * 16;
+    const uint32_t bx_full_peer = ptx::mapa(b_x_full + 8 * wg, peer);
+    const uint32_t b_xe = b_x_empty + 8 * wg;
     uint8_t* const pslot = reinterpret_cast<uint8_t*>(&S.xbuf[wg][0][0]);
     unsigned long long* const chain = &S.mchain[row];
 
@@ -797,14 +848,39 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
           ptx::tmem_ld32(t_s, r0);
           ptx::tmem_ld32(t_s + 32, r1);
           ptx::tmem_ld_wait();
+          ptx::tc_fence_before();
+          if (real) ptx::mbar_arrive(b_sfree);
 #pragma unroll
           for (int k = 0; k < 32; ++k) {
             s[k] = __uint_as_float(r0[k]);
             s[32 + k] = __uint_as_float(r1[k]);
           }
+          // ---- this tile's partial scores -> the peer: 16 values -> 12 packed words -> three
+          // 16-byte stores, four times; the slot is free once the peer's P.V of this
+          // warpgroup's previous tile has read it
+          if (send_in_softmax<KV>() && real) {
+            const int use = gg >> 1;
+            if (use >= 1 && !ptx::mbar_wait(b_xe, (use - 1) & 1, abort_flag, true)) {
+              dead = true;
+            } else {
+#pragma unroll
+              for (int h = 0; h < 4; ++h) {
+                const uint32_t* src = h < 2 ? r0 + 16 * h : r1 + 16 * (h - 2);
+                uint32_t pw[12];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  pack24x4(src[4 * j], src[4 * j + 1], src[4 * j + 2], src[4 * j + 3], pw[3 * j], pw[3 * j + 1],
+                           pw[3 * j + 2]);
+#pragma unroll
+                for (int j = 0; j < 3; ++j)
+                  ptx::st_async_v4(x_peer + (3 * h + j) * 128 * 16, __uint_as_float(pw[4 * j]),
+                                   __uint_as_float(pw[4 * j + 1]), __uint_as_float(pw[4 * j + 2]),
+                                   __uint_as_float(pw[4 * j + 3]), bx_full_peer);
+              }
+            }
+          }
         }
-        ptx::tc_fence_before();
-        if (real) ptx::mbar_arrive(b_sfree);
+        if (dead) break;
         // ---- the peer's partial scores (pushed by its senders)
         if (real && q == 0 && lane == 0) ptx::mbar_arrive_expect_tx(b_xf, kXBytes);
         if (real && !ptx::mbar_wait(b_xf, (gg >> 1) & 1, abort_flag, true)) { dead = true; break; }
@@ -1022,6 +1098,12 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       ptx::tc_fence_before();
       ptx::mbar_arrive(b_o_free);
       ++n_item;
+    }
+    // the peer's P.V commit for this warpgroup's last tile lands on x_empty[wg]: take it
+    // before exit
+    if (send_in_softmax<KV>() && !dead && g > 0) {
+      const int last = ((g - 1) & 1) == wg ? g - 1 : g - 2;
+      if (last >= 0) ptx::mbar_wait(b_xe, (uint32_t)(last >> 1) & 1u, abort_flag, true);
     }
   } else if (warp == kWarpItems) {
     // ------------------------------------------------------------------ work items
