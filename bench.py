@@ -77,12 +77,23 @@ def load_peaks():
     return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
 
 
+def _code_tokens(text: str) -> str:
+    """C++ source without comments and blank lines (string literals in these files hold no
+    comment markers), so that an edit to comments alone keeps the identity of the code."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_sha() -> str:
+    """Identity of the compiled code: a hash of the CUDA sources' code (comments excluded)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_latent_kv_split_gb300", "csrc")
     for fn in sorted(os.listdir(csrc)):
         if fn.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(csrc, fn), "rb").read())
+            h.update(fn.encode())
+            h.update(_code_tokens(open(os.path.join(csrc, fn)).read()).encode())
     return h.hexdigest()[:16]
 
 

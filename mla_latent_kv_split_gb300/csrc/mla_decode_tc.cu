@@ -19,23 +19,26 @@
 //                   E2M1 data plus E4M3 scales, into the tail of the stage)
 //   MMA warps       one issues S[128 x 64] = Q[128 x 288] (in TMEM) . K^T (18 MMAs, K = 16),
 //                   the other O[128 x 256] += P[128 x 64] (in smem) . V[64 x 256] (4 MMAs, N = 256)
-//   sender warps    one warpgroup.  (1) Prepares landed tiles for the MMAs when needed:
-//                   zeroes the rows that are masked (ragged tail, invalid page) so that
-//                   garbage, even NaN, cannot reach P.V, and for FP8 / NVFP4 decodes the raw
-//                   bytes in place into f16 (exact for both formats) in the same swizzled
-//                   layout.  (2) Thread = head row: loads the row's 64 partial scores from
-//                   TMEM and pushes them (24-bit packed) into the peer CTA's exchange buffer
-//                   with asynchronous stores that complete on the peer's mbarrier.  (3) Loads
-//                   each work item's Q into TMEM (latent) and shared memory (rope).
+//   producer warp   also zeroes the masked rows of a bf16 tile (ragged tail, invalid page)
+//                   after it lands, so that garbage, even NaN, cannot reach P.V.
+//   sender warps    one warpgroup.  (1) Loads each work item's Q into TMEM (latent) and
+//                   shared memory (rope), once the previous item's score MMAs are done.
+//                   (2) bf16 / NVFP4: thread = head row: loads the row's 64 partial scores
+//                   from TMEM and pushes them (24-bit packed) into the peer CTA's exchange
+//                   buffer with asynchronous stores that complete on the peer's mbarrier.
+//                   FP8: decodes each landed tile's E4M3 bytes in place into f16 (exact) in
+//                   the swizzled layout the MMAs read, masked rows as zeros.
 //   softmax warps   two warpgroups that take alternate tiles (even / odd), so two tiles are
 //                   in flight; thread = head row, all 64 columns of the tile.  Loads its
-//                   partial scores from TMEM, adds the peer's, takes the row max, and runs
-//                   the online softmax in base 2 with a lazy reference max: the reference
-//                   only moves (and O is rescaled) when a tile's max exceeds it by more than
-//                   8, and the two warpgroups pass it from tile to tile through shared
-//                   memory.  P (bf16 / f16) goes into the exchange slot the partial scores
-//                   arrived in; at the end of a work item both warpgroups normalise O (128
-//                   columns each) and write the output, or the split partial and its LSE.
+//                   partial scores from TMEM (FP8: and pushes them to the peer itself), adds
+//                   the peer's, takes the row max, and runs the online softmax in base 2 with
+//                   a lazy reference max: the reference only moves (and O is rescaled) when a
+//                   tile's max exceeds it by more than 8, and the two warpgroups pass it from
+//                   tile to tile through shared memory.  P (bf16 / f16) goes into the
+//                   exchange slot the partial scores arrived in; at the end of a work item
+//                   both warpgroups normalise O (128 columns each) and write the output, or
+//                   the split partial and its LSE.  NVFP4: each warpgroup decodes its own
+//                   next tile (E2M1 x E4M3 scale, exact in f16) in place.
 //
 // Tensor memory (512 columns): O [0,256) fp32; two score buffers S0 [256,320), S1 [320,384)
 // fp32 (S0 holds even tiles, S1 odd tiles); Q [384,512) bf16 pairs (this CTA's 256 latent
@@ -44,7 +47,7 @@
 // Handshakes with the peer CTA: partial scores of tile g go into the peer's exchange slot
 // g&1 (st.async, completing on the peer's x_full[g&1]); the peer's P(g) then overwrites
 // that slot, and the P.V MMAs that read it arrive, through a multicast commit, on the
-// sender's x_empty[g&1]: only then may the sender push the scores of tile g+2.
+// pushing side's x_empty[g&1]: only then may the scores of tile g+2 be pushed.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
