@@ -1,0 +1,43 @@
+"""Host-side pieces of bench.py: the algorithmic work it divides by (cache rows read once per
+request, the union of the query windows), and the code hash that keys recorded ncu traffic
+(comments do not change it, code does)."""
+import os
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from mla_latent_kv_split_gb300 import workloads as W  # noqa: E402
+
+
+def test_algorithmic_work_counts_each_cache_row_once():
+    w = W.WORKLOADS["paged_fp8"].scaled(B=3, q_len=2, H=16, seq_lens_override=(10, 300, 1))
+    inp = W.make_inputs(w)
+    nbytes, flops, kv = bench.algorithmic_work(inp)
+    assert kv == (10 + 300 + 1) * 576
+    # visible positions per query: (9, 10), (299, 300), (0, 1)
+    assert flops == 2.0 * 16 * (576 + 512) * (9 + 10 + 299 + 300 + 0 + 1)
+    io = 3 * 2 * 16 * (576 * 2 + 512 * 2 + 4)
+    table = 4 * (1 + 5 + 1) + 4 * 3
+    assert nbytes == kv + io + table
+
+
+def test_algorithmic_work_with_a_window_reads_the_union_of_the_windows():
+    w = W.WORKLOADS["paged_fp8"].scaled(B=3, q_len=2, H=16, seq_lens_override=(10, 300, 1))
+    inp = W.make_inputs(w)
+    _, flops, kv = bench.algorithmic_work(inp, window=100)
+    # request 1: query 0 sees [199, 299), query 1 [200, 300): the union is [199, 300)
+    assert kv == (10 + 101 + 1) * 576
+    assert flops == 2.0 * 16 * (576 + 512) * (9 + 10 + 100 + 100 + 0 + 1)
+
+
+def test_code_hash_ignores_comments_only():
+    a = "int f(int x) {  // the input\n  return x + 1; /* one\n more */\n}\n"
+    b = "// header\nint f(int x) {\n\n  return x + 1;\n}\n"
+    c = "int f(int x) {\n  return x + 2;\n}\n"
+    assert bench._code_tokens(a) == bench._code_tokens(b)
+    assert bench._code_tokens(a) != bench._code_tokens(c)
+    assert len(bench.kernel_source_sha()) == 16
