@@ -209,3 +209,31 @@ def test_batched_gemv_arguments_validated(L):
                        (dict(xt=100), 1), (dict(oh=500), 1), (dict(H=70000), 2), (dict(status=P + 1), 1)]:
         assert call(**over) == code, over
     assert call(T=0, x=None, w=None, out=None) == 0
+
+
+def test_binding_shape_checks_raise_before_the_library_is_called(L):
+    import torch
+    x = torch.empty((4, 2, 128), dtype=torch.bfloat16)
+    w = torch.empty((2, 64, 96), dtype=torch.bfloat16)  # K mismatch
+    with pytest.raises(ValueError):
+        mb.mla_batched_gemv(x, w, out=torch.empty((4, 2, 64), dtype=torch.bfloat16))
+    w = torch.empty((2, 64, 128), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):  # out not [T, H, N]
+        mb.mla_batched_gemv(x, w, out=torch.empty((4, 2, 65), dtype=torch.bfloat16))
+    tok = torch.empty((3, 576), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):  # rope view of the wrong width
+        mb.mla_kv_append(tok[:, :512], tok[:, 500:], torch.zeros(3, dtype=torch.int64),
+                         torch.empty((1, 64, 576), dtype=torch.bfloat16))
+    with pytest.raises(ValueError):  # slots and rows disagree
+        mb.mla_kv_append(tok[:, :512], tok[:, 512:], torch.zeros(2, dtype=torch.int64),
+                         torch.empty((1, 64, 576), dtype=torch.bfloat16))
+
+
+def test_binding_reports_library_errors_with_their_code(L):
+    # T > 0 with a null cache is rejected by the library's validation: MLAError(code 1)
+    import torch
+    tok = torch.empty((3, 576), dtype=torch.bfloat16)
+    with pytest.raises(mb.MLAError) as e:
+        mb.mla_kv_append(tok[:, :512], tok[:, 512:], torch.zeros(3, dtype=torch.int64), 0,
+                         page_size=64, num_pages=1, stream=0)
+    assert e.value.code == 1
