@@ -86,14 +86,19 @@ def _code_tokens(text: str) -> str:
     return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
 
 
+# The decode kernel's translation unit: the kernel and every header it includes.
+DECODE_SOURCES = ("mla_common.cuh", "mla_decode_tc.cu", "mla_device.cuh", "mla_ptx.cuh", "mla_tmap.cuh")
+
+
 def kernel_source_sha() -> str:
-    """Identity of the compiled code: a hash of the CUDA sources' code (comments excluded)."""
+    """Identity of the decode kernel's compiled code: a hash of its sources' code (comments
+    excluded), which keys the ncu traffic recorded for it."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_latent_kv_split_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".cuh")):
-            h.update(fn.encode())
-            h.update(_code_tokens(open(os.path.join(csrc, fn)).read()).encode())
+    for fn in DECODE_SOURCES:
+        h.update(fn.encode())
+        h.update(_code_tokens(open(os.path.join(csrc, fn)).read()).encode())
+    h.update(_code_tokens(open(os.path.join(ROOT, "include", "mla_decode.h")).read()).encode())
     return h.hexdigest()[:16]
 
 
