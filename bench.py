@@ -440,6 +440,47 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def append_cpu_baseline(x, cache_np, w, inp, seconds):
+    """The append oracle, as it stands, on the batch's tokens 64 at a time for a bounded time,
+    each chunk written into one page of a cache of the same format (the oracle returns a
+    copy of the cache it is given, so the sample's cache is kept to one page); GB/s of the
+    same algorithmic bytes per token."""
+    import numpy as np
+    from oracle import kv_append_ref
+    bits = x.view(torch_int16()).cpu().numpy().view(np.uint16)
+    page = np.zeros_like(cache_np[:1])
+    n, T = 0, bits.shape[0]
+    t0 = time.perf_counter()
+    while n < T and (n == 0 or time.perf_counter() - t0 < seconds):
+        k = min(T - n, w.page_size)
+        kv_append_ref.kv_append_ref(page, bits[n:n + k, :512], bits[n:n + k, 512:], np.arange(k), w.kv_dtype,
+                                    w.page_size, inp["kv_scale"])
+        n += k
+    el = time.perf_counter() - t0
+    per_tok = 1152 + BYTES_PER_TOKEN[w.kv_dtype] + 8
+    return {"value": n * per_tok / el / 1e9, "unit": "GB/s", "cores": cores_used(), "kind": "oracle",
+            "sample": f"{n} tokens of the same batch, {el:.2f} s, NumPy"}
+
+
+def absorb_cpu_baseline(q_raw, w_ukT, o_lat, w_uv, nbytes, seconds):
+    """The projection oracle (float64) on both projections of the same tensors, once."""
+    import numpy as np
+    from oracle import absorb_ref
+    b = lambda t: t.contiguous().view(torch_int16()).cpu().numpy().view(np.uint16)
+    xq, wq, xo, wo = b(q_raw[:, :, :128]), b(w_ukT), b(o_lat), b(w_uv)
+    t0 = time.perf_counter()
+    absorb_ref.batched_gemv_ref(xq, wq)
+    absorb_ref.batched_gemv_ref(xo, wo)
+    el = time.perf_counter() - t0
+    return {"value": nbytes / el / 1e9, "unit": "GB/s", "cores": cores_used(), "kind": "oracle",
+            "sample": f"both projections of the same step once, {el:.2f} s, float64 NumPy"}
+
+
+def torch_int16():
+    import torch
+    return torch.int16
+
+
 def run_append(args, w, inp, world, rank, dev):
     """The KV-cache append with quantise-on-write: T new tokens (bf16 [T, 576]) written to
     distinct locations of the workload's cache, in its format.  Algorithmic bytes per token:
@@ -501,6 +542,7 @@ def run_append(args, w, inp, world, rank, dev):
                      "frac": achieved / peaks["hbm"], "traffic": None, "peak_source": peaks["source"],
                      "kernel": "mla_kv_append_kernel"},
         "device_status": int(status.item()), "clocks": clocks, "gpu_launches": args.steps,
+        "cpu_baseline": append_cpu_baseline(x, cache_np, w, inp, args.cpu_seconds),
     }
     print(json.dumps(line), flush=True)
 
@@ -569,6 +611,7 @@ def run_absorb(args, w, world, rank, dev):
                      "frac": achieved / peaks["hbm"], "traffic": None, "peak_source": peaks["source"],
                      "kernel": "mla_batched_gemv_kernel x2"},
         "device_status": int(status.item()), "clocks": clocks, "gpu_launches": 2 * args.steps,
+        "cpu_baseline": absorb_cpu_baseline(q_raw, w_ukT, o_lat, w_uv, nbytes, args.cpu_seconds),
     }
     print(json.dumps(line), flush=True)
 
