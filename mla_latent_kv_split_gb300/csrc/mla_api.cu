@@ -112,8 +112,9 @@ MLA_EXPORT mla_status_t mla_decode_workspace_size(int B, int q_len, int H, int n
   if (!bytes || B < 1) return MLA_ERR_INVALID_ARG;
   mla_status_t st = check_shape(B, q_len, H, num_splits);
   if (st != MLA_OK) return st;
+  // forced splits bound the partials per (b, i) without reference to the device
   int C = 0;
-  if (current_workers(&C) != cudaSuccess) return MLA_ERR_CUDA;
+  if (num_splits == 0 && current_workers(&C) != cudaSuccess) return MLA_ERR_CUDA;
   *bytes = required_bytes(B * q_len, H, num_splits, C);
   return MLA_OK;
 }

@@ -10,8 +10,13 @@ from mla_latent_kv_split_gb300 import binding as mb
 
 # Tolerance of the decode: |out - ref| <= ATOL + RTOL*|ref| on the bf16 output and
 # |lse - ref| <= LSE_ATOL on the fp32 log-sum-exp.  Relative L2 error of the output is
-# also gated (REL_L2) to catch kernels that are wrong but inside the elementwise bound.
-ATOL, RTOL, LSE_ATOL, REL_L2 = 1e-2, 1e-2, 1e-3, 5e-3
+# also gated, over the whole output (REL_L2) and over every (b, i, h) row of 512 values
+# (ROW_REL_L2), to catch kernels that are wrong but inside the elementwise bound: one wrong
+# row among thousands stays under the tensor-wide gate, and where outputs are small (long
+# contexts, |out| ~ 0.01) the elementwise bound alone admits errors near the values
+# themselves.  The bf16 output, bf16 P and bf16 split partials each round at 2^-9
+# relative, so a correct row sits near 0.3 % (measured max below 1 %).
+ATOL, RTOL, LSE_ATOL, REL_L2, ROW_REL_L2 = 1e-2, 1e-2, 1e-3, 5e-3, 2e-2
 
 
 def ensure_built():
@@ -80,6 +85,14 @@ def assert_close(out, lse, ref_out, ref_lse, rows=None, what=""):
     empty = np.all(ref_out == 0, axis=-1)  # nothing visible (a finite sink still sets lse)
     assert np.all(out[empty] == 0), f"{what}: rows with nothing visible must be 0"
     den = np.linalg.norm(ref_out)
-    if den > 0:
-        rel = np.linalg.norm(out - ref_out) / den
-        assert rel <= REL_L2, f"{what}: rel L2 {rel:.3g}"
+    rel = np.linalg.norm(out - ref_out) / den if den > 0 else 0.0
+    # per (b, i, h) row of 512 output values
+    rn = np.linalg.norm(ref_out, axis=-1)
+    en = np.linalg.norm(out - ref_out, axis=-1)
+    live = rn > 0
+    row_rel = en[live] / rn[live] if live.any() else np.zeros(1)
+    worst_row = np.unravel_index(np.argmax(np.where(live, en / np.where(live, rn, 1.0), 0.0)), rn.shape)
+    print(f"[parity] {what}: max|err| {err.max() if err.size else 0.0:.3g}, rel L2 {rel:.3g}, "
+          f"worst row rel L2 {row_rel.max():.3g} at {worst_row}, rows {int(live.sum())}")
+    assert rel <= REL_L2, f"{what}: rel L2 {rel:.3g}"
+    assert row_rel.max() <= ROW_REL_L2, f"{what}: row rel L2 {row_rel.max():.3g} at {worst_row}"

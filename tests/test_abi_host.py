@@ -237,3 +237,11 @@ def test_binding_reports_library_errors_with_their_code(L):
         mb.mla_kv_append(tok[:, :512], tok[:, 512:], torch.zeros(3, dtype=torch.int64), 0,
                          page_size=64, num_pages=1, stream=0)
     assert e.value.code == 1
+
+
+@pytest.mark.parametrize("B,q_len,H,n", [(32, 1, 128, 5), (1, 1, 16, 2), (8, 4, 128, 3), (4, 2, 64, 3),
+                                         (1024, 1, 128, 1), (2, 8, 16, 4096)])
+def test_forced_workspace_size_is_header_plus_tokenspeed_formula(L, B, q_len, H, n):
+    # forced splits: at most n partials per (b, i), each H*(512+1) fp32 values -- the
+    # tokenspeed decode workspace formula -- after the 32 KB plan / status header
+    assert mb.mla_decode_workspace_size(B, q_len, H, n) == 32768 + oracle.workspace_bytes_formula(B, H, q_len, n)

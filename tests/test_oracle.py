@@ -444,3 +444,35 @@ def test_window_and_sink_pure_python():
         for c in range(0, 512, 41):
             o = math.fsum(math.exp(x) / z * kf[n - W_ + j][c] for j, x in enumerate(xs))
             assert abs(out[0, 0, h, c] - o) < 1e-12
+
+
+def _workspace_golden():
+    rows, bounds = [], []
+    with open(os.path.join(GOLDEN, "workspace_bytes.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].split()
+            if not line:
+                continue
+            if line[0] == "bound":
+                bounds.append(tuple(int(x) for x in line[1:]))
+            else:
+                rows.append(tuple(int(x) for x in line))
+    return rows, bounds
+
+
+def test_workspace_bytes_formula_matches_hand_worked_sizes():
+    # tokenspeed tokenspeed_mla.py, the CuteDSL decode workspace notes: B*H*q_len*split_kv*(D+1)*acc_bytes
+    rows, bounds = _workspace_golden()
+    assert len(rows) >= 4 and bounds
+    for B, H, q_len, splits, D, acc, want in rows:
+        assert oracle.workspace_bytes_formula(B, H, q_len, splits, D=D, acc_bytes=acc) == want
+    # the per-device bound of the same notes, num_SMs*H*q_len*(D+1)*4, holds whenever
+    # B*split_kv <= num_SMs, and is reached at B*split_kv == num_SMs
+    for sms, H, q_len, D, want in bounds:
+        for B in (1, 2, 5, 19, 32, 76, 152):
+            for splits in range(1, sms // B + 1):
+                assert oracle.workspace_bytes_formula(B, H, q_len, splits, D=D) <= want
+        assert oracle.workspace_bytes_formula(sms, H, q_len, 1, D=D) == want
+        assert oracle.workspace_bytes_formula(8, H, q_len, sms // 8, D=D) == want
+    # one partial of one head is the 512 output values plus its log-sum-exp
+    assert oracle.workspace_bytes_formula(1, 1, 1, 1) == (512 + 1) * 4
