@@ -277,6 +277,140 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def _roofline(nbytes: float, flops: float, t_s: float, peaks: dict) -> dict:
+    t_mem = nbytes / (peaks["hbm"] * 1e9)
+    t_mma = flops / (peaks["bf16"] * 1e12)
+    if t_mem >= t_mma:
+        roof = {"bound": "hbm", "achieved": nbytes / t_s / 1e9, "peak": peaks["hbm"], "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": flops / t_s / 1e12, "peak": peaks["bf16"], "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["peak_source"] = peaks["source"]
+    roof["roofline_us"] = 1e6 * max(t_mem, t_mma)
+    return roof
+
+
+class DecodeCase:
+    """One workload resident on the device, with a bound ``call()`` of ``mla_decode``."""
+
+    def __init__(self, w, inp, dev, window: int = 0, h_sinks=None):
+        import numpy as np
+        import torch
+        from mla_latent_kv_split_gb300 import binding as mb
+
+        self.w, self.inp, self.dev, self.window = w, inp, dev, window
+
+        def to_dev(a, bf16=False):
+            t = torch.from_numpy(a.view(np.int16) if bf16 else a)
+            return (t.view(torch.bfloat16) if bf16 else t).to(dev)
+
+        self.q_nope = to_dev(inp["q_nope"], True)
+        self.q_pe = to_dev(inp["q_pe"], True)
+        self.cache = to_dev(inp["cache"], inp["cache"].dtype == np.uint16)
+        self.table = to_dev(inp["block_table"])
+        self.seq_lens = to_dev(inp["seq_lens"])
+        self.ws = mb.alloc_workspace(w.B, w.q_len, w.H, w.num_splits, dev)
+        self.out = torch.empty((w.B, w.q_len, w.H, 512), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((w.B, w.q_len, w.H), dtype=torch.float32, device=dev)
+        self.sinks = None if h_sinks is None else torch.from_numpy(h_sinks).to(dev)
+        self.stream = torch.cuda.current_stream(dev)
+
+    def call(self, q_nope=None, q_pe=None, table=None, seq_lens=None):
+        from mla_latent_kv_split_gb300 import binding as mb
+        w = self.w
+        mb.mla_decode(self.q_nope if q_nope is None else q_nope, self.q_pe if q_pe is None else q_pe, self.cache,
+                      self.table if table is None else table, self.seq_lens if seq_lens is None else seq_lens,
+                      w.sm_scale, w.kv_dtype, self.inp["kv_scale"], w.num_splits, page_size=w.page_size,
+                      num_pages=self.inp["num_pages"], workspace=self.ws, out=self.out, lse=self.lse,
+                      stream=self.stream, window=self.window, sinks=self.sinks)
+
+
+def make_l2_flush(dev):
+    import torch
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_head = flush[: flush.numel() // 2]
+
+    def l2_flush():
+        # Write 512 MB (evicts every line of the call's inputs and outputs), then read the
+        # first 256 MB back so that the lines left in L2 are clean: the timed call then does
+        # not pay for writing back the flush buffer's dirty lines.
+        flush.zero_()
+        flush_head.sum()
+    return l2_flush
+
+
+def time_calls(case, l2_flush, steps: int, warmup: int, barrier=None):
+    """Warm-up calls, then `steps` calls each timed with CUDA events on the launching stream,
+    L2 flushed before each.  Returns (times in ms, device status of the last call)."""
+    import torch
+    from mla_latent_kv_split_gb300 import binding as mb
+    t_warm = time.perf_counter()
+    k = 0
+    while k < max(3, warmup) or time.perf_counter() - t_warm < 0.3:
+        l2_flush()
+        case.call()
+        torch.cuda.synchronize()
+        k += 1
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    for s in range(steps):
+        l2_flush()
+        evs[s][0].record(case.stream)
+        case.call()
+        evs[s][1].record(case.stream)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    # the status word of the last timed call; a call that hit a bounded wait shows as a
+    # time outlier (the waits give up after seconds)
+    status = mb.mla_decode_read_status(case.ws)
+    times_ms = [a.elapsed_time(b) for a, b in evs]
+    if status or max(times_ms) > 20 * statistics.median(times_ms):
+        print(f"bench.py: {case.w.name}: device status {status:#x}, slowest call {max(times_ms):.3f} ms",
+              file=sys.stderr)
+    return times_ms, status
+
+
+def cpu_baseline_entry(inp, seconds: float, window: int = 0, sinks=None) -> dict:
+    w = inp["workload"]
+    cpu_kv, cpu_el, cpu_req, cpu_rows = cpu_oracle_sample(inp, seconds, window=window, sinks=sinks)
+    return {"value": cpu_kv / cpu_el / 1e9, "unit": "GB/s", "cores": cores_used(), "kind": "oracle",
+            "sample": f"{cpu_req} whole requests ({cpu_rows} (b,i) rows x {w.H} heads) of the same "
+                      f"workload, {cpu_el:.1f} s, float64 NumPy"}
+
+
+def measure_config(name: str, dev, l2_flush, steps: int, warmup: int, cpu_seconds: float, index: int) -> dict:
+    """All of one workload's figures, measured in this run: µs per call (mean, median,
+    max), KV GB/s, TFLOP/s, the roofline fraction, ncu DRAM traffic when recorded for these
+    kernel sources, the SM clocks seen while timing, and the oracle on a bounded sample."""
+    import torch
+    from mla_latent_kv_split_gb300 import workloads as W
+    w = W.WORKLOADS[name]
+    inp = W.make_inputs(w)
+    nbytes, flops, kv_bytes = algorithmic_work(inp)
+    case = DecodeCase(w, inp, dev)
+    sampler = ClockSampler(index)
+    sampler.start()
+    times_ms, status = time_calls(case, l2_flush, steps, warmup)
+    clocks = sampler.stop()
+    del case
+    torch.cuda.empty_cache()
+    t_s = sum(times_ms) / len(times_ms) * 1e-3
+    roof = _roofline(nbytes, flops, t_s, load_peaks())
+    roof["traffic"] = traffic_for(name)
+    return {
+        "config": workload_config(w, "flushed between steps"),
+        "us_per_call": 1e6 * t_s, "us_per_call_median": 1e3 * statistics.median(times_ms),
+        "us_per_call_max": 1e3 * max(times_ms), "steps": len(times_ms),
+        "kv_gbs": kv_bytes / t_s / 1e9, "tflops": flops / t_s / 1e12,
+        "algorithmic_bytes": nbytes, "algorithmic_flops": flops, "device_status": status,
+        "roofline": roof, "clocks": clocks, "gpu_launches": 2 * len(times_ms),
+        "cpu_baseline": cpu_baseline_entry(inp, cpu_seconds),
+    }
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -288,9 +422,11 @@ def run_ours(args):
 
     if rank == 0:
         build.build()
+    barrier = None
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
+        barrier = dist.barrier
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = W.WORKLOADS[args.workload]
@@ -301,65 +437,14 @@ def run_ours(args):
         return run_absorb(args, w, world, rank, dev)
     nbytes, flops, kv_bytes = algorithmic_work(inp, args.window)
     h_sinks = W.draw_sinks(w.H, seed=0) if args.sinks else None
+    case = DecodeCase(w, inp, dev, args.window, h_sinks)
+    l2_flush = make_l2_flush(dev)
+    stream = case.stream
+    smi_index = local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0
 
-    def to_dev(a, bf16=False):
-        t = torch.from_numpy(a.view(np.int16) if bf16 else a)
-        return (t.view(torch.bfloat16) if bf16 else t).to(dev)
-
-    q_nope = to_dev(inp["q_nope"], True)
-    q_pe = to_dev(inp["q_pe"], True)
-    cache = to_dev(inp["cache"], inp["cache"].dtype == np.uint16)
-    table = to_dev(inp["block_table"])
-    seq_lens = to_dev(inp["seq_lens"])
-    ws = mb.alloc_workspace(w.B, w.q_len, w.H, w.num_splits, dev)
-    out = torch.empty((w.B, w.q_len, w.H, 512), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((w.B, w.q_len, w.H), dtype=torch.float32, device=dev)
-    sinks = None if h_sinks is None else torch.from_numpy(h_sinks).to(dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    flush_head = flush[: flush.numel() // 2]
-
-    def l2_flush():
-        # Write 512 MB (evicts every line of the call's inputs and outputs), then read the
-        # first 256 MB back so that the lines left in L2 are clean: the timed call then does
-        # not pay for writing back the flush buffer's dirty lines.
-        flush.zero_()
-        flush_head.sum()
-
-    stream = torch.cuda.current_stream(dev)
-
-    def call():
-        mb.mla_decode(q_nope, q_pe, cache, table, seq_lens, w.sm_scale, w.kv_dtype, inp["kv_scale"],
-                      w.num_splits, page_size=w.page_size, num_pages=inp["num_pages"], workspace=ws, out=out,
-                      lse=lse, stream=stream, window=args.window, sinks=sinks)
-
-    sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    sampler = ClockSampler(smi_index)
     sampler.start()
-    t_warm = time.perf_counter()
-    k = 0
-    while k < max(3, args.warmup) or time.perf_counter() - t_warm < 0.3:
-        l2_flush()
-        call()
-        torch.cuda.synchronize()
-        k += 1
-    status = mb.mla_decode_read_status(ws)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    for s in range(args.steps):
-        l2_flush()
-        evs[s][0].record(stream)
-        call()
-        evs[s][1].record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    # the status word of the last timed call; a call that hit a bounded wait shows as a
-    # time outlier (the waits give up after seconds)
-    status = mb.mla_decode_read_status(ws)
-    times_ms = [a.elapsed_time(b) for a, b in evs]
-    if status or max(times_ms) > 20 * statistics.median(times_ms):
-        print(f"bench.py: device status {status:#x}, slowest call {max(times_ms):.3f} ms", file=sys.stderr)
+    times_ms, status = time_calls(case, l2_flush, args.steps, args.warmup, barrier)
     clocks = sampler.stop()
     t_mean = sum(times_ms) / len(times_ms)
 
@@ -382,12 +467,9 @@ def run_ours(args):
         d_qp.copy_(h_qp, non_blocking=True)
         d_bt.copy_(h_bt, non_blocking=True)
         d_sl.copy_(h_sl, non_blocking=True)
-        mb.mla_decode(d_qn.view(torch.bfloat16), d_qp.view(torch.bfloat16), cache, d_bt, d_sl, w.sm_scale,
-                      w.kv_dtype, inp["kv_scale"], w.num_splits, page_size=w.page_size,
-                      num_pages=inp["num_pages"], workspace=ws, out=out, lse=lse, stream=stream,
-                      window=args.window, sinks=sinks)
-        h_out.copy_(out.view(torch.int16), non_blocking=True)
-        h_lse.copy_(lse, non_blocking=True)
+        case.call(d_qn.view(torch.bfloat16), d_qp.view(torch.bfloat16), d_bt, d_sl)
+        h_out.copy_(case.out.view(torch.int16), non_blocking=True)
+        h_lse.copy_(case.lse, non_blocking=True)
         b.record(stream)
         torch.cuda.synchronize()
         if s >= args.warmup:
@@ -401,19 +483,12 @@ def run_ours(args):
 
     peaks = load_peaks()
     t_s = t_mean * 1e-3
-    t_mem = nbytes / (peaks["hbm"] * 1e9)
-    t_mma = flops / (peaks["bf16"] * 1e12)
-    if t_mem >= t_mma:
-        roof = {"bound": "hbm", "achieved": nbytes / t_s / 1e9, "peak": peaks["hbm"], "unit": "GB/s"}
-    else:
-        roof = {"bound": "tensor", "achieved": flops / t_s / 1e12, "peak": peaks["bf16"], "unit": "TFLOP/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = traffic_for(w.name)
-    roof["peak_source"] = peaks["source"]
-    roof["roofline_us"] = 1e6 * max(t_mem, t_mma)
+    roof = _roofline(nbytes, flops, t_s, peaks)
+    roof["traffic"] = traffic_for(w.name) if not (args.window or args.sinks) else None
     roof["kernel"] = "mla_decode call (decode kernel + split-K combine)"
+    del case
+    torch.cuda.empty_cache()
 
-    cpu_kv, cpu_el, cpu_req, cpu_rows = cpu_oracle_sample(inp, args.cpu_seconds, window=args.window, sinks=h_sinks)
     line = {
         "metric": METRIC, "value": job_rate(kv_bytes, t_s, world) / 1e9, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_mean, "higher_is_better": True,
@@ -425,9 +500,7 @@ def run_ours(args):
         "kv_gbs": kv_bytes / t_s / 1e9, "tflops": flops / t_s / 1e12,
         "algorithmic_bytes": nbytes, "algorithmic_flops": flops, "device_status": status,
         "roofline": roof,
-        "cpu_baseline": {"value": cpu_kv / cpu_el / 1e9, "unit": "GB/s", "cores": cores_used(), "kind": "oracle",
-                         "sample": f"{cpu_req} whole requests ({cpu_rows} (b,i) rows x {w.H} heads) of the same "
-                                   f"workload, {cpu_el:.1f} s, float64 NumPy"},
+        "cpu_baseline": cpu_baseline_entry(inp, args.cpu_seconds, args.window, h_sinks),
         "e2e": {"value": job_rate(kv_bytes, e2e_mean * 1e-3, world) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_mean,
                 "note": "q_nope, q_pe, block_table, seq_lens copied in from pinned host memory and out, lse "
@@ -435,6 +508,12 @@ def run_ours(args):
         "clocks": clocks,
         "gpu_launches": 2 * args.steps,
     }
+    if args.configs == "all" and world == 1 and not (args.window or args.sinks):
+        # every workload of the path, each timed in this same run (the headline one again,
+        # so that each entry comes from one uniform procedure)
+        line["configs"] = {name: measure_config(name, dev, l2_flush, args.steps, args.warmup,
+                                                min(args.cpu_seconds, 3.0), smi_index)
+                           for name in W.WORKLOADS}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -628,6 +707,8 @@ def main():
     ap.add_argument("--sinks", action="store_true", help="per-head attention sinks")
     ap.add_argument("--op", default="decode", choices=["decode", "kv_append", "absorb"])
     ap.add_argument("--append-tokens", type=int, default=0, help="kv_append: tokens per call (default B*q_len)")
+    ap.add_argument("--configs", default="all", choices=["all", "none"],
+                    help="decode: also time every workload in this run (one entry per workload under 'configs')")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

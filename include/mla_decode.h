@@ -32,8 +32,12 @@
  *     out) set bits of a status word in the workspace instead of trapping; the affected
  *     tokens are skipped.  mla_decode_read_status returns the word.
  *   - All work is enqueued on `stream`; the call is safe to capture in a CUDA graph.
- *   - Thread safety: no mutable global state besides a per-device cache of the SM
- *     count and of the kernel attributes, filled once under a lock.
+ *   - Thread safety: the library's mutable global state is a per-device cache of the
+ *     SM count and of the kernel attributes, and (mla_decode_no_alloc only) a per-device
+ *     cache of its scratch buffer's address, each filled once under a lock, plus that
+ *     scratch buffer itself: one per device, shared by every mla_decode_no_alloc call, so
+ *     those calls must be ordered by the caller (see mla_decode_no_alloc).  Every other
+ *     entry point touches only the caller's buffers.
  */
 #ifndef MLA_DECODE_H_
 #define MLA_DECODE_H_
@@ -72,7 +76,7 @@ typedef enum {
 #define MLA_STATUS_SEQ_LT_QLEN 0x4u       /* seq_len < q_len (early queries see nothing) */
 #define MLA_STATUS_NEG_SEQ_LEN 0x8u       /* seq_len < 0 (treated as 0) */
 #define MLA_STATUS_WAIT_TIMEOUT 0x10u     /* a bounded in-kernel wait gave up */
-#define MLA_STATUS_Q_RANGE 0x20u          /* |q| beyond fp16 range on an FP8/NVFP4 cache */
+#define MLA_STATUS_Q_RANGE 0x20u          /* a non-finite q value (FP8/NVFP4 caches; the row is not finite) */
 #define MLA_STATUS_SLOT_OUT_OF_RANGE 0x40u /* mla_kv_append: a location past the cache (skipped) */
 
 /* Limits of this build. */

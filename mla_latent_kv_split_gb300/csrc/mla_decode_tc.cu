@@ -88,6 +88,13 @@ constexpr float kRescaleThreshold = 8.0f;       // log2 units: P stays below 2^8
 // slot is free again once every reader took it: the producer warp, the two MMA issuers,
 // the 4 sender warps and the 8 softmax warps.
 constexpr int kItemRing = 16;
+// Quantized caches: the senders publish each item's q row exponents through a ring of this
+// many slots.  The senders load item k's q only after every score MMA of item k-1 completed,
+// and the score MMA of a tile waits until its buffer's softmax warpgroup read the scores
+// two tiles earlier, so when item k's exponents are written both softmax warpgroups have
+// started item k-4 at least (they pass each other only at an item's epilogue): the slot of
+// item k-4 has been read.
+constexpr int kQExpRing = 4;
 constexpr uint32_t kItemReaders = 15;
 
 // warp roles
@@ -151,6 +158,7 @@ struct Bars {
   uint64_t x_full[2];          // the peer's partial scores landed in my exchange slot (tx count)
   uint64_t x_empty[2];         // the peer's P.V read its slot: I may push the next scores into it
   uint64_t ep;                 // both softmax warpgroups published their (max, sum) of an item
+  uint64_t qs_ready[kQExpRing];  // quantized caches: the senders wrote an item's q row exponents
   uint64_t mma_final;          // every score MMA of this CTA completed
   uint64_t mma_final_pv;       // every P.V MMA of this CTA completed
   uint64_t item_full[kItemRing];   // ring slot holds the next work item
@@ -172,6 +180,7 @@ struct Smem {
   int items_min[kItemRing];        // the item's unit's first attended position (sliding window)
   float ep_m[2][2][128];           // [item parity][warpgroup][row] reference max
   float ep_l[2][2][128];           // [item parity][warpgroup][row] row sum relative to it
+  int8_t qexp[kQExpRing][128];     // quantized caches: [item % ring][row] exponent e of the item's q row
   unsigned long long tmask[kStages];  // rows of the staged tile that are real, visible positions
   uint32_t tmem_base;
   int abort_flag;
@@ -216,13 +225,30 @@ __device__ __forceinline__ TileInfo tile_info(const DecodeParams& p, int b, int 
 }
 __device__ __forceinline__ bool tile_needs_fixup(const TileInfo& ti) { return ti.rowmask != ~0ull; }
 
-// Two bf16 values -> two f16 (exact for |x| in [2^-14, 65504]; smaller magnitudes round to
-// f16 subnormals, larger ones overflow and are reported).
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v, bool& out_of_range) {
-  const float lo = __uint_as_float(v << 16), hi = __uint_as_float(v & 0xFFFF0000u);
-  out_of_range |= fabsf(lo) > 65504.f || fabsf(hi) > 65504.f;
-  return ptx::pack_f16x2(lo, hi);
+// Quantized caches multiply in f16, so each (item, head) row of q is converted from bf16 to
+// f16 as q * 2^-e, e chosen per row and per CTA from the row's largest magnitude over the
+// CTA's 288 columns: e = 0 while that maximum lies in [2^-8, 2^15) (the usual range: the
+// conversion is then the plain one), else the power of two that brings it into
+// [2^14, 2^15).  Multiplying by a power of two is exact, so every value within 2^-29 of
+// the row's maximum converts exactly and none overflows; the partial scores, computed on
+// the scaled row, are multiplied back by 2^e in fp32 (exact) before the two CTAs' halves
+// are added.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v, float mul) {
+  return ptx::pack_f16x2(__uint_as_float(v << 16) * mul, __uint_as_float(v & 0xFFFF0000u) * mul);
 }
+// Largest bf16 magnitude (as bits) of the two halves of v, folded into m.
+__device__ __forceinline__ uint32_t bf16x2_absmax_bits(uint32_t v, uint32_t m) {
+  return max(m, max(v & 0x7FFFu, (v >> 16) & 0x7FFFu));
+}
+// The row exponent e of a row whose largest magnitude has bf16 bits m (non-finite rows: 0).
+__device__ __forceinline__ int q_row_exponent(uint32_t m) {
+  if (m == 0u || m >= 0x7F80u) return 0;
+  const int E = (m < 0x80u) ? -127 : (int)(m >> 7) - 127;  // floor(log2 max); subnormals below 2^-126
+  if (E >= -8 && E <= 14) return 0;
+  return min(113, max(-100, E - 14));
+}
+// 2^k as a float, k in [-126, 127].
+__device__ __forceinline__ float pow2f(int k) { return __uint_as_float((uint32_t)(k + 127) << 23); }
 
 // Four fp32 bit patterns -> three words holding their top 24 bits (sign, exponent, 15
 // mantissa bits): w0 = a.hi16 | b.hi16 << 16, w1 = c.hi16 | d.hi16 << 16, w2 = the third
@@ -392,6 +418,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
   const uint32_t b_mma_final = ptx::smem_u32(&S.bars.mma_final);
   const uint32_t b_mma_final_pv = ptx::smem_u32(&S.bars.mma_final_pv);
   const uint32_t b_ep = ptx::smem_u32(&S.bars.ep);
+  const uint32_t b_qs_ready = ptx::smem_u32(&S.bars.qs_ready[0]);
   const uint32_t b_item_full = ptx::smem_u32(&S.bars.item_full[0]), b_item_empty = ptx::smem_u32(&S.bars.item_empty[0]);
 
   if (tid == 0) {
@@ -409,6 +436,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
     }
     for (int s = 0; s < 4; ++s) ptx::mbar_init(b_o_done + 8 * s, 1);
     ptx::mbar_init(b_q_ready, kSenderThreads);
+    for (int s = 0; s < kQExpRing; ++s) ptx::mbar_init(b_qs_ready + 8 * s, kSenderThreads);
     ptx::mbar_init(b_q_free, 1);  // one commit per item, after its last score MMAs
     ptx::mbar_init(b_o_free, kSoftmaxThreads);
     ptx::mbar_init(b_ep, kSoftmaxThreads);
@@ -625,6 +653,10 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
     const uint32_t t_s0 = tmem + lane_off + kTmemS, t_q = tmem + lane_off + kTmemQ;
     const uint32_t x_peer = ptx::mapa(ptx::smem_u32(&S.xbuf[0][0][0]), peer);
     const uint32_t bx_full_peer = ptx::mapa(b_x_full, peer);
+    // Quantized caches: the power of two this thread's row of the current item's q was
+    // divided by (1 when unscaled), and whether any row of this warp was scaled.
+    float q_sc = 1.f;
+    bool q_scaled = false;
 
     // (2) Tile k's partial scores -> the peer CTA.
     auto send = [&](int k) -> bool {
@@ -637,6 +669,13 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       ptx::tmem_ld_wait();
       ptx::tc_fence_before();
       ptx::mbar_arrive(b_s_free + 8 * (k & 1));
+      if (KV != MLA_KV_BF16 && q_scaled) {  // back to the scale of the unscaled row (exact)
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          r0[j] = __float_as_uint(__uint_as_float(r0[j]) * q_sc);
+          r1[j] = __float_as_uint(__uint_as_float(r1[j]) * q_sc);
+        }
+      }
       const int slot = k & 1, use = k >> 1;
       // the peer's P.V(k-2) has read the slot (its P) before the next scores go in
       if (use >= 1 && !ptx::mbar_wait(b_x_empty + 8 * slot, (use - 1) & 1, abort_flag, true)) return false;
@@ -665,12 +704,10 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       const int b = w.u / p.q_len, i = w.u % p.q_len;
       return ((size_t)b * p.q_len + i) * p.H + (row < p.H ? row : 0);
     };
-    auto load_q = [&](const WorkItem& w) {
-      const bool real = row < p.H;
-      const size_t qrow = q_row(w);
-      const uint4* qn = reinterpret_cast<const uint4*>(p.q_nope + qrow * kLatent + 256 * cr);
-      const uint4* qp = reinterpret_cast<const uint4*>(p.q_pe + qrow * kRope + 32 * cr);
-      bool q_range = false;
+    // One pass over the row: q * mul -> TMEM / shared memory; returns the row's largest
+    // bf16 magnitude (as bits).
+    auto store_q = [&](const uint4* qn, const uint4* qp, bool real, float mul) -> uint32_t {
+      uint32_t mx = 0u;
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
         uint4 x[16];
@@ -688,7 +725,10 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
           }
           if (KV != MLA_KV_BF16) {
 #pragma unroll
-            for (int k = 0; k < 32; ++k) v[k] = bf16x2_to_f16x2(v[k], q_range);
+            for (int k = 0; k < 32; ++k) {
+              mx = bf16x2_absmax_bits(v[k], mx);
+              v[k] = bf16x2_to_f16x2(v[k], mul);
+            }
           }
           ptx::tmem_st32(t_q + 64 * half + 32 * c, v);
         }
@@ -697,14 +737,39 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       for (int c = 0; c < 4; ++c) {
         uint4 x = real ? __ldg(qp + c) : make_uint4(0u, 0u, 0u, 0u);
         if (KV != MLA_KV_BF16) {
-          x.x = bf16x2_to_f16x2(x.x, q_range);
-          x.y = bf16x2_to_f16x2(x.y, q_range);
-          x.z = bf16x2_to_f16x2(x.z, q_range);
-          x.w = bf16x2_to_f16x2(x.w, q_range);
+          mx = bf16x2_absmax_bits(x.w, bf16x2_absmax_bits(x.z, bf16x2_absmax_bits(x.y, bf16x2_absmax_bits(x.x, mx))));
+          x.x = bf16x2_to_f16x2(x.x, mul);
+          x.y = bf16x2_to_f16x2(x.y, mul);
+          x.z = bf16x2_to_f16x2(x.z, mul);
+          x.w = bf16x2_to_f16x2(x.w, mul);
         }
         *reinterpret_cast<uint4*>(S.q_rope + row * 64 + ((c ^ ((row >> 1) & 3)) * 16)) = x;
       }
-      if (q_range) set_status(&S.status, MLA_STATUS_Q_RANGE);
+      return mx;
+    };
+    // Q of item k: this row's 256 latent columns -> TMEM, 32 rope columns -> shared memory
+    // (64-byte swizzled K-major layout: chunk c of row r sits at chunk position c ^ ((r >> 1)
+    // & 3) of the row's 64 bytes).  Quantized caches: converted to f16 as they are; a warp
+    // holding a row whose maximum falls outside the plain range stores its rows again,
+    // scaled, and the exponents go to the softmax warpgroups through the exponent ring.
+    auto load_q = [&](const WorkItem& w, int k) {
+      const bool real = row < p.H;
+      const size_t qrow = q_row(w);
+      const uint4* qn = reinterpret_cast<const uint4*>(p.q_nope + qrow * kLatent + 256 * cr);
+      const uint4* qp = reinterpret_cast<const uint4*>(p.q_pe + qrow * kRope + 32 * cr);
+      const uint32_t mx = store_q(qn, qp, real, 1.f);
+      if (KV != MLA_KV_BF16) {
+        const int e = q_row_exponent(mx);
+        if (mx >= 0x7F80u) set_status(&S.status, MLA_STATUS_Q_RANGE);
+        q_scaled = __any_sync(0xffffffffu, e != 0);
+        if (q_scaled) {
+          ptx::tmem_st_wait();
+          store_q(qn, qp, real, pow2f(-e));
+        }
+        q_sc = pow2f(e);
+        S.qexp[k % kQExpRing][row] = (int8_t)e;
+        ptx::mbar_arrive(b_qs_ready + 8 * (k % kQExpRing));
+      }
       ptx::fence_proxy_async_smem();
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
@@ -720,7 +785,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       const int tq = (warp - kWarpSender0) * 32 + lane;
       // the first item's unit is known from the schedule: its Q loads overlap the item ring's
       // start and the first cache loads
-      if (wst.busy) load_q(WorkItem{wst.u0, 0, 0, -1, 0});
+      if (wst.busy) load_q(WorkItem{wst.u0, 0, 0, -1, 0}, 0);
       for (int k_item = 0; !dead; ++k_item) {
         const int got = item_take(S.items, S.items_min, b_item_full, b_item_empty, k_item, abort_flag, it, true);
         if (got <= 0) {
@@ -734,7 +799,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
             break;
           }
           ptx::tc_fence_after();
-          load_q(it);
+          load_q(it, k_item);
         }
         if (decode_in_senders<KV>()) {
           for (int t = 0; t < nt; ++t)
@@ -755,7 +820,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       const int tq = (warp - kWarpSender0) * 32 + lane;
       // the first item's unit is known from the schedule: its Q loads overlap the item ring's
       // start and the first cache loads
-      if (wst.busy) load_q(WorkItem{wst.u0, 0, 0, -1, 0});
+      if (wst.busy) load_q(WorkItem{wst.u0, 0, 0, -1, 0}, 0);
       for (int k_item = 0; !dead; ++k_item) {
         const int got = item_take(S.items, S.items_min, b_item_full, b_item_empty, k_item, abort_flag, it, true);
         if (got <= 0) {
@@ -775,7 +840,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
             dead = true;
             break;
           }
-          if (t0 == it.tok_lo && g > 0) load_q(it);
+          if (t0 == it.tok_lo && g > 0) load_q(it, k_item);
         }
       }
       if (!dead && g > 0 && send(g - 1)) {
@@ -839,6 +904,19 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
         dead = true;
         break;
       }
+      // quantized caches: the exponent this CTA's half of the item's q row was scaled by
+      float q_sc = 1.f;
+      bool q_scaled = false;
+      if (KV != MLA_KV_BF16) {
+        const int qs = k_item % kQExpRing;
+        if (!ptx::mbar_wait(b_qs_ready + 8 * qs, (uint32_t)(k_item / kQExpRing) & 1u, abort_flag)) {
+          dead = true;
+          break;
+        }
+        const int e = S.qexp[qs][row];
+        q_sc = pow2f(e);
+        q_scaled = __any_sync(0xffffffffu, e != 0);
+      }
       for (; t_idx < nt; t_idx += 2) {
         const bool real = t_idx >= 0;
         const int gg = g0 + t_idx;
@@ -853,6 +931,13 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
           ptx::tmem_ld_wait();
           ptx::tc_fence_before();
           if (real) ptx::mbar_arrive(b_sfree);
+          if (KV != MLA_KV_BF16 && q_scaled) {  // back to the scale of the unscaled row (exact)
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              r0[k] = __float_as_uint(__uint_as_float(r0[k]) * q_sc);
+              r1[k] = __float_as_uint(__uint_as_float(r1[k]) * q_sc);
+            }
+          }
 #pragma unroll
           for (int k = 0; k < 32; ++k) {
             s[k] = __uint_as_float(r0[k]);
