@@ -38,10 +38,17 @@ def _deps():
         os.path.join(ROOT, "include", "mla_decode.h"), os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+# A test build of the same sources (never loaded by the package): every bounded wait gives
+# up after 20 ms instead of 4 s (and a waiting warp sleeps at most 0.1 ms at a time), and the exported mla_fault_injection_drop_tile makes one
+# CTA leave one tile unloaded, so that tests can run the kernel's abort path.
+FAULT_LIB = os.path.join(LIBDIR, "libmla_decode_fault_injection.so")
+FAULT_FLAGS = ("-DMLA_FAULT_INJECTION", "-DMLA_WAIT_LIMIT_NS=20000000ull", "-DMLA_SUSPEND_HINT_NS=100000u")
+
+
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
@@ -50,16 +57,20 @@ def flags(extra=()):
                    "-I", os.path.join(ROOT, "include"), "--expt-relaxed-constexpr", *extra]
 
 
-def build(verbose: bool = False, force: bool = False, extra=()) -> str:
-    if not force and up_to_date():
-        return LIB
+def build(verbose: bool = False, force: bool = False, extra=(), fault_injection: bool = False) -> str:
+    lib = FAULT_LIB if fault_injection else LIB
+    builddir = BUILDDIR + ("_fault_injection" if fault_injection else "")
+    if fault_injection:
+        extra = (*extra, *FAULT_FLAGS)
+    if not force and up_to_date(lib):
+        return lib
     os.makedirs(LIBDIR, exist_ok=True)
-    os.makedirs(BUILDDIR, exist_ok=True)
+    os.makedirs(builddir, exist_ok=True)
     cc = nvcc()
     objs = []
 
     def compile_one(src):
-        obj = os.path.join(BUILDDIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(builddir, os.path.basename(src)[:-3] + ".o")
         cmd = [cc, *flags(extra), "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
@@ -73,13 +84,13 @@ def build(verbose: bool = False, force: bool = False, extra=()) -> str:
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -99,7 +99,7 @@ mla_batched_gemv_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
     }
     // loads still in flight after an abort land before the CTA exits
     for (int k = max(0, kc - stages); k < kc; ++k)
-      ptx::mbar_wait(ptx::smem_u32(&C.full[k % stages]), (k / stages) & 1, abort_flag, false, 100000000ull);
+      ptx::mbar_drain(ptx::smem_u32(&C.full[k % stages]), (k / stages) & 1);
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer: D[128 rows x tt tokens] += W[128 x 64] . X[tt x 64]^T per chunk
     const uint32_t idesc = ptx::idesc_f16(1, 0, kBlockM, (uint32_t)tt);

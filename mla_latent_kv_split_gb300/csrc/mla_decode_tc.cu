@@ -61,6 +61,13 @@
 #include "mla_tmap.cuh"
 
 namespace mla {
+#ifdef MLA_FAULT_INJECTION
+// Test builds only (never compiled into the shipped library): the producer of CTA
+// g_drop_cta leaves tile g_drop_tile of its schedule unloaded, so that the waits on that
+// tile run out and the kernel takes its abort path.
+__device__ int g_drop_cta = -1;
+__device__ int g_drop_tile = -1;
+#endif
 namespace tc {
 
 constexpr int kThreads = 512;
@@ -280,7 +287,7 @@ __device__ __forceinline__ bool chain_wait(const unsigned long long* slot, unsig
     if ((unsigned)(v >> 32) == g) return true;
     if ((it & 255u) == 0) {
       if (*abort_flag) return false;
-      if (ptx::globaltimer_ns() - t0 > 4000000000ull) {
+      if (ptx::globaltimer_ns() - t0 > ptx::kWaitLimitNs) {
         *abort_flag = 1;
         return false;
       }
@@ -495,6 +502,12 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
           dead = true;
           break;
         }
+#ifdef MLA_FAULT_INJECTION
+        if (blockIdx.x == (unsigned)g_drop_cta && g == g_drop_tile) {
+          if (leader) S.tmask[st] = ti.rowmask;
+          continue;  // neither the expected byte count nor the loads: kv_full never completes
+        }
+#endif
         if (leader) {
           uint32_t bytes = 0;
           for (int j = 0; j < ti.npages; ++j) {
@@ -549,7 +562,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
     if (leader) {
       for (int k = 1; k <= kStages && g - k >= 0; ++k) {
         const int gg = g - k;
-        ptx::mbar_wait(b_kv_full + 8 * (gg % kStages), (gg / kStages) & 1, abort_flag, false, 100000000ull);
+        ptx::mbar_drain(b_kv_full + 8 * (gg % kStages), (gg / kStages) & 1);
       }
     }
   } else if (warp == kWarpMma) {
@@ -607,7 +620,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
         ++n_item;
       }
       ptx::mma_commit(b_mma_final);
-      ptx::mbar_wait(b_mma_final, 0, abort_flag, false, 100000000ull);
+      ptx::mbar_drain(b_mma_final, 0);
     }
   } else if (warp == kWarpMmaPv) {
     // ------------------------------------------------------------------ P.V MMA issuer
@@ -642,7 +655,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
         ++n_item;
       }
       ptx::mma_commit(b_mma_final_pv);
-      ptx::mbar_wait(b_mma_final_pv, 0, abort_flag, false, 100000000ull);
+      ptx::mbar_drain(b_mma_final_pv, 0);
     }
   } else if (warp >= kWarpSender0 && warp < kWarpSoftmax0) {
     // ------------------------------------------------------------------ senders
@@ -708,13 +721,16 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
     // bf16 magnitude (as bits).
     auto store_q = [&](const uint4* qn, const uint4* qp, bool real, float mul) -> uint32_t {
       uint32_t mx = 0u;
+      // 16-byte loads in flight per round: 32 (two TMEM stores) with the wider register
+      // budgets, 8 (one store) with the narrowest
+      constexpr int kLd = RegSplit<KV>::sender >= 112 ? 16 : 8;
 #pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-        uint4 x[16];
+      for (int part = 0; part < 32 / kLd; ++part) {
+        uint4 x[kLd];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) x[k] = real ? __ldg(qn + 16 * half + k) : make_uint4(0u, 0u, 0u, 0u);
+        for (int k = 0; k < kLd; ++k) x[k] = real ? __ldg(qn + kLd * part + k) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < kLd / 8; ++c) {
           uint32_t v[32];
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
@@ -730,7 +746,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
               v[k] = bf16x2_to_f16x2(v[k], mul);
             }
           }
-          ptx::tmem_st32(t_q + 64 * half + 32 * c, v);
+          ptx::tmem_st32(t_q + (kLd * part + 8 * c) * 4, v);
         }
       }
 #pragma unroll
@@ -1270,6 +1286,16 @@ bool encode_rows_map(CUtensorMap* m, const void* base, size_t rows, int elem_byt
 }  // namespace
 
 size_t tc_smem_bytes() { return sizeof(tc::Smem) + 1024; }
+
+#ifdef MLA_FAULT_INJECTION
+// Test builds only: makes CTA `cta` skip the loads of tile `tile` of its schedule in the
+// following decode launches (cta < 0: no tile skipped).
+extern "C" __attribute__((visibility("default"))) int mla_fault_injection_drop_tile(int cta, int tile) {
+  cudaError_t e = cudaMemcpyToSymbol(g_drop_cta, &cta, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_drop_tile, &tile, sizeof(int));
+  return (int)e;
+}
+#endif
 
 // Largest number of 2-CTA clusters of the tensor-core kernel that can be co-resident (the
 // three cache formats share block size and shared memory).

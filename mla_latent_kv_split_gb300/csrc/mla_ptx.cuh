@@ -22,7 +22,12 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // ------------------------------------------------------------------ mbarrier
 // try_wait may suspend the waiting warp for up to this long; it resumes as soon as the phase
 // completes.  Suspension keeps waiting warps from flooding the shared-memory pipe with polls.
-constexpr uint32_t kSuspendHintNs = 10000000u;
+// (A phase that never completes is noticed after 64 such suspensions at most; the test
+// build with short wait limits shortens the hint with them.)
+#ifndef MLA_SUSPEND_HINT_NS
+#define MLA_SUSPEND_HINT_NS 10000000u
+#endif
+constexpr uint32_t kSuspendHintNs = MLA_SUSPEND_HINT_NS;
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
@@ -80,10 +85,20 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   return ok != 0;
 }
 
+// Limit of every bounded wait on another role's progress (4 s of %globaltimer).  A test
+// build of the library shortens it to make a wait run out quickly.
+#ifndef MLA_WAIT_LIMIT_NS
+#define MLA_WAIT_LIMIT_NS 4000000000ull
+#endif
+constexpr uint64_t kWaitLimitNs = MLA_WAIT_LIMIT_NS;
+// Limit of a drain: the wait, on the way out, for this CTA's own asynchronous copies or
+// MMAs already in flight (they complete within microseconds unless they were never issued).
+constexpr uint64_t kDrainLimitNs = 100000000ull;
+
 // Bounded wait: returns false (and raises the CTA's abort flag) when the phase has not
 // completed within `limit_ns` or when another role of the CTA already aborted.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          bool cluster_scope = false, uint64_t limit_ns = 4000000000ull) {
+                                          bool cluster_scope = false, uint64_t limit_ns = kWaitLimitNs) {
   if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
@@ -95,6 +110,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
         return false;
       }
     }
+  }
+}
+
+// Drain: bounded wait for this CTA's own asynchronous work already in flight, which the
+// abort flag does not cut short (that work lands in this CTA's memory, so the CTA must not
+// exit first); returns false after kDrainLimitNs (work that was never issued).
+__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > kDrainLimitNs) return false;
   }
 }
 
@@ -120,6 +147,12 @@ __device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, float a, floa
                                             uint32_t cluster_bar) {
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
                ::"r"(cluster_addr), "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_bar)
+               : "memory");
+}
+// Asynchronous 4-byte store into another CTA's shared memory, counted like st_async_v4.
+__device__ __forceinline__ void st_async_b32(uint32_t cluster_addr, uint32_t v, uint32_t cluster_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
+               ::"r"(cluster_addr), "r"(v), "r"(cluster_bar)
                : "memory");
 }
 // Barrier over a subset of the CTA's warps (ids 1..15; 0 is __syncthreads).
@@ -368,6 +401,12 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
+}
+// Two f16 (low half first) -> two fp32, exact.
+__device__ __forceinline__ void unpack_f16x2(uint32_t v, float& lo, float& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(v));
 }
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   uint32_t r;
