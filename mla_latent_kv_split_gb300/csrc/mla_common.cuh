@@ -74,6 +74,16 @@ MLA_HD int unit_tile0(int vis, int window) { return window_first(vis, window) / 
 MLA_HD int unit_tiles(int vis, int window) { return vis > 0 ? cdiv_i(vis, kTile) - unit_tile0(vis, window) : 0; }
 
 // ---- heuristic mode (num_splits == 0): contiguous, balanced ranges per worker ----
+// Units are laid end to end in schedule order.  With q_len == 1 that is the unit order.
+// With q_len > 1 it is query-major (position k = i * B + b holds unit (b, i)): the q_len
+// queries of a request then sit at the same offsets of q_len nearly equal stretches of the
+// schedule, so that (with a worker count divisible by q_len) the workers serving the
+// different queries of a request walk the same pages at the same time and all but the
+// first of each page's reads come from L2.
+MLA_HD bool query_major(int q_len, int num_splits) { return q_len > 1 && num_splits == 0; }
+MLA_HD int unit_at(int k, int B, int q_len, int num_splits) {
+  return query_major(q_len, num_splits) ? (k % B) * q_len + k / B : k;
+}
 // Every unit with visible KV is laid out as kItemCost placeholder slots (the fixed cost of
 // starting a work item on it: its query load, pipeline refill and epilogue, measured at
 // about four tiles' time) followed by its tiles.  With N slots in all and C workers, only
@@ -104,12 +114,14 @@ struct UnitPlan {
 };
 
 // Host evaluation of the whole plan (the device kernels evaluate the same formulas with a
-// block-wide scan).  Returns the number of partial slots used.
+// block-wide scan).  plan[] is indexed by unit; tile_begin and the partial slots follow the
+// schedule order.  Returns the number of partial slots used.
 inline int plan_host(const int32_t* seq_lens, int B, int q_len, int max_pages, int page_size,
                      int num_splits, int C, UnitPlan* plan, int window = 0) {
   const int U = B * q_len;
   long long N = 0;
-  for (int u = 0; u < U; ++u) {
+  for (int k = 0; k < U; ++k) {
+    const int u = unit_at(k, B, q_len, num_splits);
     int b = u / q_len, i = u % q_len;
     int L = clamp_seq_len(seq_lens[b], max_pages, page_size);
     int vis = unit_visible(L, q_len, i);
@@ -127,7 +139,8 @@ inline int plan_host(const int32_t* seq_lens, int B, int q_len, int max_pages, i
   }
   int slots = 0;
   const int Ca = active_workers(N, C);
-  for (int u = 0; u < U; ++u) {
+  for (int k = 0; k < U; ++k) {
+    const int u = unit_at(k, B, q_len, num_splits);
     if (num_splits == 0) {
       if (plan[u].tiles == 0) {
         plan[u].parts = 0;

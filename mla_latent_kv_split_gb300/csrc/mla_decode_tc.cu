@@ -402,18 +402,6 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
   volatile int* abort_flag = &S.abort_flag;
 
   asm volatile("griddepcontrol.launch_dependents;");
-  {
-    // the schedule is evaluated in the exchange buffers, which are idle until the first tile
-    PlanSmem& plan = *reinterpret_cast<PlanSmem*>(&S.xbuf[0][0][0]);
-    if (tid == 0) S.status = 0u;
-    __syncthreads();
-    compute_plan(p, plan, S.scratch, &S.status, blockIdx.x == 0);
-    if (tid == 0) S.wstart = worker_start(p, plan, worker);
-    __syncthreads();
-  }
-  const WorkerStart& wst = S.wstart;  // read from shared memory where needed
-  const int n_tiles_total = wst.N;
-
   const uint32_t b_kv_full = ptx::smem_u32(&S.bars.kv_full[0]);
   const uint32_t b_kv_ready = ptx::smem_u32(&S.bars.kv_ready[0]);
   const uint32_t b_kv_empty = ptx::smem_u32(&S.bars.kv_empty[0]);
@@ -428,7 +416,11 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
   const uint32_t b_qs_ready = ptx::smem_u32(&S.bars.qs_ready[0]);
   const uint32_t b_item_full = ptx::smem_u32(&S.bars.item_full[0]), b_item_empty = ptx::smem_u32(&S.bars.item_empty[0]);
 
+  // Set-up that does not depend on the schedule, ahead of it: barriers, tensor memory, the
+  // tensor maps, and an L2 prefetch of this CTA's share of the block table (the first tiles'
+  // page numbers are then read from L2 once the schedule is known).
   if (tid == 0) {
+    S.status = 0u;
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(b_kv_full + 8 * s, 1);
       ptx::mbar_init(b_kv_ready + 8 * s, KV == MLA_KV_BF16 ? 1 : kWgThreads);
@@ -465,10 +457,33 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
     ptx::prefetch_tmap(&tm_lat);
     ptx::prefetch_tmap(&tm_rope);
   }
+  if (warp == kWarpMmaPv && lane == 0) {
+    const size_t table = (size_t)p.B * p.max_pages * 4 & ~(size_t)15;
+    const size_t share = (((table + gridDim.x - 1) / gridDim.x) + 15) & ~(size_t)15;
+    const size_t lo = (size_t)blockIdx.x * share;
+    if (lo < table)
+      ptx::bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(p.block_table) + lo, (uint32_t)min(share, table - lo));
+  }
+  __syncthreads();
+  {
+    // the schedule is evaluated in the exchange buffers, which are idle until the first tile
+    PlanSmem& plan = *reinterpret_cast<PlanSmem*>(&S.xbuf[0][0][0]);
+    compute_plan(p, plan, S.scratch, &S.status, blockIdx.x == 0);
+    if (tid == 0) {
+      S.wstart = worker_start(p, plan, worker);
+      // the first item's query rows, on their way to L2 before the roles start
+      if (S.wstart.busy && cr == 0) {
+        ptx::bulk_prefetch_l2(p.q_nope + (size_t)S.wstart.u0 * p.H * kLatent, (uint32_t)p.H * kLatent * 2);
+        ptx::bulk_prefetch_l2(p.q_pe + (size_t)S.wstart.u0 * p.H * kRope, (uint32_t)p.H * kRope * 2);
+      }
+    }
+  }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::cluster_sync_all();  // the peer's barriers exist before any remote arrive
   ptx::tc_fence_after();
+  const WorkerStart& wst = S.wstart;  // read from shared memory where needed
+  const int n_tiles_total = wst.N;
   const uint32_t tmem = S.tmem_base;
   if (warp == kWarpProducer) {
     regs_to<RegSplit<KV>::ctrl>();

@@ -70,10 +70,11 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits_rn(float f) {
 }
 
 // ---------------------------------------------------------------- schedule on the device
+// Indexed by schedule position k (unit unit_at(k)).
 struct PlanSmem {
   int N;                     // total tiles (heuristic) or items (forced)
   int begin[kMaxUnits + 1];  // exclusive prefix of tiles / items
-  int vis[kMaxUnits];        // visible positions per unit
+  int vis[kMaxUnits];        // visible positions of the unit
   int slot[kMaxUnits];       // first partial slot or -1
   int pref[kMaxUnits];       // exclusive prefix of the partial slots of split units
 };
@@ -127,7 +128,8 @@ __device__ inline void compute_plan(const DecodeParams& p, PlanSmem& pl, int* sc
   const int tid = threadIdx.x + blockDim.x * (threadIdx.y + blockDim.y * threadIdx.z);
   const int U = p.B * p.q_len;
   unsigned bad = 0;
-  for (int u = tid; u < U; u += T) {
+  for (int k = tid; k < U; k += T) {
+    const int u = unit_at(k, p.B, p.q_len, p.num_splits);
     int b = u / p.q_len, i = u % p.q_len;
     int raw = __ldg(p.seq_lens + b);
     if (raw < 0) bad |= MLA_STATUS_NEG_SEQ_LEN;
@@ -135,9 +137,9 @@ __device__ inline void compute_plan(const DecodeParams& p, PlanSmem& pl, int* sc
     int L = clamp_seq_len(raw, p.max_pages, p.page_size);
     if (L < p.q_len && i == 0) bad |= MLA_STATUS_SEQ_LT_QLEN;
     int vis = unit_visible(L, p.q_len, i);
-    pl.vis[u] = vis;
+    pl.vis[k] = vis;
     int tiles = unit_tiles(vis, p.window);
-    pl.begin[u] = p.num_splits > 0
+    pl.begin[k] = p.num_splits > 0
                       ? (tiles ? cdiv_i(tiles, forced_span_tiles(tiles, p.num_splits)) : 0)
                       : unit_slots(tiles);
   }
@@ -151,34 +153,34 @@ __device__ inline void compute_plan(const DecodeParams& p, PlanSmem& pl, int* sc
   __syncthreads();
   // parts per unit -> slot scan (reuse pl.slot as the per-unit split-part count)
   const int Ca = active_workers(N, p.workers);
-  for (int u = tid; u < U; u += T) {
+  for (int k = tid; k < U; k += T) {
     int parts;
     if (p.num_splits > 0) {
-      parts = pl.begin[u + 1] - pl.begin[u];
+      parts = pl.begin[k + 1] - pl.begin[k];
     } else {
       // a unit's tiles are the last of its slots
-      parts = pl.begin[u + 1] > pl.begin[u]
-                  ? worker_of(pl.begin[u + 1] - 1, N, Ca) - worker_of(pl.begin[u] + kItemCost, N, Ca) + 1
+      parts = pl.begin[k + 1] > pl.begin[k]
+                  ? worker_of(pl.begin[k + 1] - 1, N, Ca) - worker_of(pl.begin[k] + kItemCost, N, Ca) + 1
                   : 0;
     }
-    pl.slot[u] = parts > 1 ? parts : 0;
+    pl.slot[k] = parts > 1 ? parts : 0;
     if (write_plan) {
       int2* plan = reinterpret_cast<int2*>(p.ws + kPlanOffset);
-      plan[u].x = parts;  // slot written below
+      plan[unit_at(k, p.B, p.q_len, p.num_splits)].x = parts;  // slot written below
     }
   }
   __syncthreads();
   block_exclusive_scan(pl.slot, U, scratch);
-  for (int u = tid; u < U; u += T) pl.pref[u] = pl.slot[u];
-  for (int u = tid; u < U; u += T) {
-    int parts = p.num_splits > 0 ? pl.begin[u + 1] - pl.begin[u]
-              : (pl.begin[u + 1] > pl.begin[u]
-                     ? worker_of(pl.begin[u + 1] - 1, N, Ca) - worker_of(pl.begin[u] + kItemCost, N, Ca) + 1
+  for (int k = tid; k < U; k += T) pl.pref[k] = pl.slot[k];
+  for (int k = tid; k < U; k += T) {
+    int parts = p.num_splits > 0 ? pl.begin[k + 1] - pl.begin[k]
+              : (pl.begin[k + 1] > pl.begin[k]
+                     ? worker_of(pl.begin[k + 1] - 1, N, Ca) - worker_of(pl.begin[k] + kItemCost, N, Ca) + 1
                      : 0);
-    if (parts <= 1) pl.slot[u] = -1;
+    if (parts <= 1) pl.slot[k] = -1;
     if (write_plan) {
       int2* plan = reinterpret_cast<int2*>(p.ws + kPlanOffset);
-      plan[u].y = pl.slot[u];
+      plan[unit_at(k, p.B, p.q_len, p.num_splits)].y = pl.slot[k];
     }
   }
   __syncthreads();
@@ -209,13 +211,14 @@ __device__ __forceinline__ int upper_bound_i(const int* a, int n, int x) {
 // evaluated here as well, from the plan, so that it is known before any cursor runs.
 struct WorkerStart {
   int u0, base0, slot0, N;
+  int k0;          // schedule position of unit u0
   int busy;        // the worker has at least one item
   WorkItem first;  // its first item (when busy)
 };
 
 __device__ inline WorkerStart worker_start(const DecodeParams& p, const PlanSmem& pl, int c) {
   const int U = p.B * p.q_len;
-  WorkerStart w{0, 0, 0, pl.N, 0, WorkItem{0, 0, 0, -1, 0}};
+  WorkerStart w{0, 0, 0, pl.N, 0, 0, WorkItem{0, 0, 0, -1, 0}};
   if (pl.N <= 0) return w;
   int first;
   int Ca = 0;
@@ -227,18 +230,20 @@ __device__ inline WorkerStart worker_start(const DecodeParams& p, const PlanSmem
     first = (int)worker_begin(c, pl.N, Ca);
   }
   if (first >= pl.N) return w;
-  const int u = upper_bound_i(pl.begin, U + 1, first) - 1;
+  const int kp = upper_bound_i(pl.begin, U + 1, first) - 1;
+  const int u = unit_at(kp, p.B, p.q_len, p.num_splits);
   w.u0 = u;
-  w.base0 = pl.begin[u];
-  w.slot0 = pl.pref[u];
+  w.k0 = kp;
+  w.base0 = pl.begin[kp];
+  w.slot0 = pl.pref[kp];
   w.busy = 1;
-  const int vis = pl.vis[u], tiles = unit_tiles(vis, p.window);
+  const int vis = pl.vis[kp], tiles = unit_tiles(vis, p.window);
   const int t0 = unit_tile0(vis, p.window), tmin = window_first(vis, p.window);
   if (p.num_splits > 0) {  // item `first` is part k of unit u
     const int k = first - w.base0;
     const int span = forced_span_tiles(tiles, p.num_splits);
     const int lo = k * span, hi = min((k + 1) * span, tiles);
-    w.first = WorkItem{u, (t0 + lo) * kTile, min((t0 + hi) * kTile, vis), pl.slot[u] >= 0 ? pl.slot[u] + k : -1, tmin};
+    w.first = WorkItem{u, (t0 + lo) * kTile, min((t0 + hi) * kTile, vis), pl.slot[kp] >= 0 ? pl.slot[kp] + k : -1, tmin};
   } else {  // the unit's tiles inside [first, end of the worker's range)
     const long long e = worker_begin(c + 1, pl.N, Ca);
     const long long r0 = (long long)w.base0 + kItemCost;  // the unit's first tile
@@ -248,7 +253,7 @@ __device__ inline WorkerStart worker_start(const DecodeParams& p, const PlanSmem
       return w;
     }
     w.first = WorkItem{u, (t0 + (int)(lo - r0)) * kTile, min((t0 + (int)(hi - r0)) * kTile, vis),
-                       pl.slot[u] >= 0 ? pl.slot[u] + (c - worker_of(r0, pl.N, Ca)) : -1, tmin};
+                       pl.slot[kp] >= 0 ? pl.slot[kp] + (c - worker_of(r0, pl.N, Ca)) : -1, tmin};
   }
   return w;
 }
@@ -261,7 +266,7 @@ __device__ __forceinline__ int unit_visible_dev(const DecodeParams& p, int u) {
 // Worker c's items one at a time, in for_each_item's order, walking units from the worker's
 // start and reading only seq_lens.  A copy of a cursor looks ahead without disturbing it.
 struct ItemCursor {
-  int u, sacc, j, ib, c;
+  int k, sacc, j, ib, c;  // k: schedule position of the current unit
   long long tb, t, e;
   bool live;
 };
@@ -270,7 +275,7 @@ __device__ inline ItemCursor item_cursor(const DecodeParams& p, const WorkerStar
   ItemCursor k{};
   k.c = c;
   k.live = w.N > 0;
-  k.u = w.u0;
+  k.k = w.k0;
   k.sacc = w.slot0;
   if (!k.live) return k;
   if (p.num_splits > 0) {
@@ -295,27 +300,28 @@ __device__ inline bool next_item(const DecodeParams& p, int N, ItemCursor& k, Wo
   if (p.num_splits > 0) {
     if (k.j >= N) return false;
     int vis, tiles, parts, span;
-    for (;;) {
-      vis = unit_visible_dev(p, k.u);
+    for (;;) {  // forced mode: schedule position = unit
+      vis = unit_visible_dev(p, k.k);
       tiles = unit_tiles(vis, p.window);
       span = forced_span_tiles(tiles, p.num_splits);
       parts = tiles ? cdiv_i(tiles, span) : 0;
       if (k.ib + parts > k.j) break;
       k.sacc += parts > 1 ? parts : 0;
       k.ib += parts;
-      ++k.u;
+      ++k.k;
     }
     const int q = k.j - k.ib;
     const int lo = q * span, hi = min((q + 1) * span, tiles);
     const int t0 = unit_tile0(vis, p.window);
-    it = WorkItem{k.u, (t0 + lo) * kTile, min((t0 + hi) * kTile, vis), parts > 1 ? k.sacc + q : -1,
+    it = WorkItem{k.k, (t0 + lo) * kTile, min((t0 + hi) * kTile, vis), parts > 1 ? k.sacc + q : -1,
                   window_first(vis, p.window)};
     k.j += p.workers;
     return true;
   }
   const int Ca = active_workers(N, p.workers);
   while (k.t < k.e) {
-    const int vis = unit_visible_dev(p, k.u);
+    const int u = unit_at(k.k, p.B, p.q_len, p.num_splits);
+    const int vis = unit_visible_dev(p, u);
     const int tiles = unit_tiles(vis, p.window);
     const long long te = k.tb + unit_slots(tiles);  // the unit's slots end
     const long long r0 = k.tb + kItemCost;          // its first tile
@@ -324,14 +330,14 @@ __device__ inline bool next_item(const DecodeParams& p, int N, ItemCursor& k, Wo
     const bool emit = tiles > 0 && hi > lo;
     if (emit) {
       const int t0 = unit_tile0(vis, p.window);
-      it = WorkItem{k.u, (t0 + (int)(lo - r0)) * kTile, min((t0 + (int)(hi - r0)) * kTile, vis),
+      it = WorkItem{u, (t0 + (int)(lo - r0)) * kTile, min((t0 + (int)(hi - r0)) * kTile, vis),
                     parts > 1 ? k.sacc + (k.c - worker_of(r0, N, Ca)) : -1, window_first(vis, p.window)};
     }
     k.t = max(k.t, min(k.e, te));
     if (k.t >= te) {
       k.sacc += parts > 1 ? parts : 0;
       k.tb = te;
-      ++k.u;
+      ++k.k;
     }
     if (emit) return true;
   }

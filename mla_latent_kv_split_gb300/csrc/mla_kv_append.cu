@@ -11,6 +11,9 @@
 //          (element 2j in the low nibble of byte j, one 8-byte store), the scale byte in the
 //          page's scale section.  A group whose scale is 0 stores zero codes.
 // Conversions use the hardware's round-to-nearest-even, saturating (satfinite) converts.
+// Quotients are the correctly rounded fp32 x / d, computed as x * r with r the correctly
+// rounded reciprocal of d and one correction step (Markstein's method): the remainder
+// x - q*d is exact by FMA and q + remainder * r rounds to the nearest quotient.
 // HBM-bound; at a decode step's few hundred tokens, launch-latency-bound.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -48,6 +51,20 @@ __device__ __forceinline__ uint32_t e2m1x8(const float* x) {
       : "=r"(d)
       : "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]), "f"(x[7]));
   return d;
+}
+
+// x / d rounded to nearest even, for d > 0 finite and r = RN(1 / d) (Markstein's final
+// step).  An exact quotient (zero remainder: zeros keep their sign) and a non-finite first
+// approximation (an infinite x) are returned as they are.
+__device__ __forceinline__ float div_rn_by(float x, float d, float r) {
+  const float q0 = x * r;
+  const float e = fmaf(-q0, d, x);
+  return (e == 0.f || !isfinite(q0)) ? q0 : fmaf(e, r, q0);
+}
+__device__ __forceinline__ float rcp_rn(float d) {
+  float r;
+  asm("rcp.rn.f32 %0, %1;" : "=f"(r) : "f"(d));
+  return r;
 }
 
 // Value of one E4M3 code (exact: every E4M3 value is an f16 value).
@@ -93,23 +110,25 @@ mla_kv_append_kernel(const uint16_t* __restrict__ latent, long long latent_strid
     }
   }
   if (kv_dtype == MLA_KV_FP8_E4M3) {
+    const float r = rcp_rn(kv_scale);
     uint32_t w[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k)
-      w[k] = e4m3x2(__fdiv_rn(x[4 * k], kv_scale), __fdiv_rn(x[4 * k + 1], kv_scale)) |
-             (e4m3x2(__fdiv_rn(x[4 * k + 2], kv_scale), __fdiv_rn(x[4 * k + 3], kv_scale)) << 16);
+      w[k] = e4m3x2(div_rn_by(x[4 * k], kv_scale, r), div_rn_by(x[4 * k + 1], kv_scale, r)) |
+             (e4m3x2(div_rn_by(x[4 * k + 2], kv_scale, r), div_rn_by(x[4 * k + 3], kv_scale, r)) << 16);
     *reinterpret_cast<uint4*>(cache + (size_t)slot * MLA_CACHE_DIM + 16 * g) = make_uint4(w[0], w[1], w[2], w[3]);
     return;
   }
   float amax = 0.f;
 #pragma unroll
   for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(x[k]));
-  const uint32_t s_code = e4m3x2(__fdiv_rn(amax, 6.f), 0.f) & 0xFFu;
+  const uint32_t s_code = e4m3x2(div_rn_by(amax, 6.f, rcp_rn(6.f)), 0.f) & 0xFFu;
   const float sv = e4m3_value(s_code);
   uint32_t d0 = 0u, d1 = 0u;
   if (sv > 0.f) {
+    const float r = rcp_rn(sv);
 #pragma unroll
-    for (int k = 0; k < 16; ++k) x[k] = __fdiv_rn(x[k], sv);
+    for (int k = 0; k < 16; ++k) x[k] = div_rn_by(x[k], sv, r);
     d0 = e2m1x8(x);
     d1 = e2m1x8(x + 8);
   }

@@ -82,9 +82,14 @@ def _check_plan(seq_lens, q_len, ps, num_splits, C, max_pages=None, window=0):
     first = np.array([oracle.window_range(int(v), window)[0] for v in vis])
     tiles = np.where(vis > 0, -(-vis // 64) - first // 64, 0)
     assert np.array_equal(pl["tiles"], tiles)
-    # slots: contiguous, disjoint, only for split units
+    # schedule order: query-major for a verify batch in the heuristic mode (position
+    # k = i * B + b holds unit (b, i)), else the unit order
+    B = len(seq_lens)
+    order = [(k % B) * q_len + k // B for k in range(U)] if (q_len > 1 and num_splits == 0) else list(range(U))
+    assert sorted(order) == list(range(U))
+    # slots: contiguous, disjoint, only for split units, in schedule order
     used = 0
-    for u in range(U):
+    for u in order:
         if pl["parts"][u] > 1:
             assert pl["slot"][u] == used
             used += pl["parts"][u]
@@ -111,7 +116,7 @@ def _check_plan(seq_lens, q_len, ps, num_splits, C, max_pages=None, window=0):
         for c in range(Ca):
             owner[c * N // Ca:(c + 1) * N // Ca] = c
         t0 = 0
-        for u in range(U):
+        for u in order:
             if tiles[u]:
                 assert pl["tile_begin"][u] == t0
                 real = owner[t0 + ITEM_COST:t0 + ITEM_COST + tiles[u]]
@@ -245,3 +250,33 @@ def test_forced_workspace_size_is_header_plus_tokenspeed_formula(L, B, q_len, H,
     # forced splits: at most n partials per (b, i), each H*(512+1) fp32 values -- the
     # tokenspeed decode workspace formula -- after the 32 KB plan / status header
     assert mb.mla_decode_workspace_size(B, q_len, H, n) == 32768 + oracle.workspace_bytes_formula(B, H, q_len, n)
+
+
+def test_verify_batch_schedule_aligns_the_queries_of_a_request(L):
+    # The NVFP4 verify workload's shape: 8 requests x 4 queries of 131,072 positions on 76
+    # workers.  In query-major order the workers serving query i of a request cover the same
+    # tiles as those serving query 0, 19 workers further on, so that a page read for one
+    # query is still in L2 when the others read it.
+    B, q_len, C, S = 8, 4, 76, 131072
+    seq = np.full(B, S, dtype=np.int32)
+    pl = _check_plan(seq, q_len, 64, 0, C)
+    tiles = pl["tiles"]
+    slots = np.where(tiles > 0, tiles + ITEM_COST, 0)
+    order = [(k % B) * q_len + k // B for k in range(B * q_len)]
+    N = int(slots.sum())
+    ranges = {}
+    for c in range(C):
+        lo, hi = c * N // C, (c + 1) * N // C
+        for u in order:
+            r0 = pl["tile_begin"][u] + ITEM_COST
+            a, b = max(lo, r0), min(hi, r0 + tiles[u])
+            if a < b:
+                ranges.setdefault(c, []).append((u // q_len, u % q_len, a - r0, b - r0))
+    per = C // q_len
+    for c in range(per):
+        for i in range(1, q_len):
+            mine, theirs = ranges[c], ranges[c + i * per]
+            assert len(mine) == len(theirs)
+            for (b0, i0, a0, e0), (b1, i1, a1, e1) in zip(mine, theirs):
+                assert b0 == b1 and i0 == 0 and i1 == i
+                assert abs(a0 - a1) <= 1 and abs(e0 - e1) <= 1

@@ -120,3 +120,67 @@ def test_append_then_decode(kv_dtype, num_splits):
     inp2 = dict(inp)
     inp2["cache"] = new_cache
     assert_close(out, lse, *oracle_ref(inp2), what=f"append+decode {kv_dtype}")
+
+
+def _every_finite_bf16(shuffle_seed=None):
+    """All 65,280 finite bf16 bit patterns (both zeros, subnormals, up to +-max), as
+    [T, 576] token rows, padded with zeros."""
+    b = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    b = b[(b & 0x7F80) != 0x7F80]
+    if shuffle_seed is not None:
+        b = np.random.default_rng(shuffle_seed).permutation(b)
+    T = -(-b.size // 576)
+    out = np.zeros(T * 576, np.uint16)
+    out[:b.size] = b
+    return out.reshape(T, 576)
+
+
+def _append_both(kv_dtype, bits, kv_scale, ps=64):
+    T = bits.shape[0]
+    num_pages = -(-T // ps)
+    slots = np.arange(T, dtype=np.int64)
+    cache = _empty_cache(kv_dtype, num_pages, ps, 0)
+    ref = KA.kv_append_ref(cache, bits[:, :512], bits[:, 512:], slots, kv_dtype, ps, kv_scale)
+    x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+    dcache = _to_dev_cache(cache)
+    mb.mla_kv_append(x[:, :512], x[:, 512:], torch.from_numpy(slots).cuda(), dcache, page_size=ps,
+                     kv_dtype=kv_dtype, kv_scale=kv_scale, num_pages=num_pages)
+    torch.cuda.synchronize()
+    return _from_dev_cache(dcache, cache), ref
+
+
+@pytest.mark.parametrize("kv_scale", [1.0, 0.05, 1.0 / 3.0, 0.0123456789, 2.0 ** -7, 3.7, 448.0 / 3.0, 1e-30, 1e30])
+def test_fp8_append_every_bf16_value(kv_scale):
+    # every finite bf16 value divided by the scale and rounded to E4M3: the quotient the
+    # kernel forms (reciprocal and one correction step) must be the correctly rounded one
+    # wherever that decides the code, so every stored byte equals the oracle's
+    got, ref = _append_both("fp8", _every_finite_bf16(), np.float32(kv_scale).item())
+    assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} bytes differ"
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_nvfp4_append_every_bf16_value(seed):
+    # every finite bf16 value, sorted by magnitude into groups of 15 neighbours, each group
+    # completed by a 16th value that sets its block scale at 1 to 12 times the group's
+    # largest (so x / scale covers every E2M1 code): the scale E4M3(amax / 6) and each code
+    # E2M1(x / scale) as the oracle's
+    b = _every_finite_bf16().reshape(-1)
+    v = torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).float().numpy()
+    v = v[np.argsort(np.abs(v), kind="stable")]
+    rng = np.random.default_rng(seed)
+    n = -(-v.size // 15)
+    vals = np.zeros(n * 15, np.float32)
+    vals[:v.size] = v * np.where(rng.random(v.size) < 0.5, -1.0, 1.0)
+    groups = np.zeros((n, 16), np.float32)
+    groups[:, 1:] = vals.reshape(n, 15)
+    factors = np.array([1.0, 1.3, 1.7, 2.3, 3.0, 4.0, 5.5, 7.5, 12.0], np.float32)
+    with np.errstate(over="ignore"):
+        setter = np.abs(groups[:, 1:]).max(axis=1) * factors[rng.integers(0, factors.size, n)]
+    groups[:, 0] = np.minimum(setter, np.float32(3.3895314e38))  # the largest finite bf16
+    x = torch.from_numpy(groups.reshape(-1))
+    T = -(-x.numel() // 576)
+    flat = torch.zeros(T * 576)
+    flat[:x.numel()] = x
+    bits = flat.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).reshape(T, 576)
+    got, ref = _append_both("nvfp4", bits, 1.0)
+    assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} bytes differ"
