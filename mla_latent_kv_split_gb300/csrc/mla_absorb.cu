@@ -69,6 +69,11 @@ mla_batched_gemv_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
     ptx::tma_load_3d(a + kABytes, &tm_x, kc * kBlockK, h, t0, full);
   };
   const int first = nk < stages ? nk : stages;
+  // Programmatic dependent launch: the next kernel on the stream may start its own
+  // set-up now; this one reads the activations (and writes its output) only after
+  // griddepcontrol.wait, i.e. once the kernel before it has completed.  The weights are
+  // not produced by that kernel, so the first ring's weight loads leave before the wait.
+  asm volatile("griddepcontrol.launch_dependents;");
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       ptx::mbar_init(ptx::smem_u32(&C.full[s]), 1);
@@ -77,9 +82,19 @@ mla_batched_gemv_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
     ptx::mbar_init(ptx::smem_u32(&C.done), 1);
     C.abort = 0;
     ptx::fence_mbar_init_cluster();
-    // the first ring's worth of loads leaves before the TMEM allocation and the block barrier
-    for (int kc = 0; kc < first; ++kc) issue(kc);
+    // the first ring's worth of loads leaves before the TMEM allocation and the block
+    // barrier: its weight chunks at once, its token chunks once the previous kernel is done
+    for (int kc = 0; kc < first; ++kc) {
+      const uint32_t a = smem0 + (kc % stages) * stage_bytes(tt), full = ptx::smem_u32(&C.full[kc % stages]);
+      ptx::mbar_arrive_expect_tx(full, stage_bytes(tt));
+      ptx::tma_load_2d(a, &tm_w, kc * kBlockK, h * N + n0, full);
+    }
   }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0)
+    for (int kc = 0; kc < first; ++kc)
+      ptx::tma_load_3d(smem0 + (kc % stages) * stage_bytes(tt) + kABytes, &tm_x, kc * kBlockK, h, t0,
+                       ptx::smem_u32(&C.full[kc % stages]));
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(&C.tmem), ncols);
     ptx::tmem_relinquish();
@@ -216,10 +231,18 @@ cudaError_t launch_batched_gemv(const uint16_t* x, long long x_token_stride, lon
       opted_in[dev] = true;
     }
   }
-  dim3 grid((N + gemv::kBlockM - 1) / gemv::kBlockM, H, (T + tt - 1) / tt);
-  kern<<<grid, gemv::kThreads, smem, stream>>>(tm_w, tm_x, out, out_token_stride, out_head_stride, T, N, K, tt, stages,
-                                               status);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((N + gemv::kBlockM - 1) / gemv::kBlockM, H, (T + tt - 1) / tt);
+  cfg.blockDim = dim3(gemv::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see griddepcontrol in the kernel
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tm_w, tm_x, out, (long long)out_token_stride, (long long)out_head_stride, T, N,
+                            K, tt, stages, status);
 }
 
 }  // namespace mla
