@@ -28,17 +28,19 @@
 //                   buffer with asynchronous stores that complete on the peer's mbarrier.
 //                   FP8: decodes each landed tile's E4M3 bytes in place into f16 (exact) in
 //                   the swizzled layout the MMAs read, masked rows as zeros.
-//   softmax warps   two warpgroups that take alternate tiles (even / odd), so two tiles are
-//                   in flight; thread = head row, all 64 columns of the tile.  Loads its
-//                   partial scores from TMEM (FP8: and pushes them to the peer itself), adds
-//                   the peer's, takes the row max, and runs the online softmax in base 2 with
-//                   a lazy reference max: the reference only moves (and O is rescaled) when a
-//                   tile's max exceeds it by more than 8, and the two warpgroups pass it from
-//                   tile to tile through shared memory.  P (bf16 / f16) goes into the
-//                   exchange slot the partial scores arrived in; at the end of a work item
-//                   both warpgroups normalise O (128 columns each) and write the output, or
-//                   the split partial and its LSE.  NVFP4: each warpgroup decodes its own
-//                   next tile (E2M1 x E4M3 scale, exact in f16) in place.
+//   softmax warps   two warpgroups; thread = head row.  bf16 / NVFP4: both take every
+//                   tile, 32 of its 64 columns each, and the two halves of a row exchange
+//                   their maxima through shared memory.  FP8: they take alternate tiles
+//                   (even / odd), all 64 columns, so two tiles are in flight.  A thread loads
+//                   its partial scores from TMEM (FP8: and pushes them to the peer itself),
+//                   adds the peer's, takes the row max, and runs the online softmax in base 2
+//                   with a lazy reference max: the reference only moves (and O is rescaled)
+//                   when a tile's max exceeds it by more than 8 (alternate tiles pass it from
+//                   one warpgroup to the other through shared memory).  P (bf16 / f16) goes
+//                   into the exchange slot the partial scores arrived in; at the end of a
+//                   work item both warpgroups normalise O (128 columns each) and write the
+//                   output, or the split partial and its LSE.  NVFP4: the two warpgroups
+//                   decode the tiles (E2M1 x E4M3 scale, exact in f16) in place, two ahead.
 //
 // Tensor memory (512 columns): O [0,256) fp32; two score buffers S0 [256,320), S1 [320,384)
 // fp32 (S0 holds even tiles, S1 odd tiles); Q [384,512) bf16 pairs (this CTA's 256 latent
@@ -107,13 +109,13 @@ constexpr uint32_t kItemReaders = 15;
 // warp roles
 constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpMmaPv = 2, kWarpItems = 3, kWarpSender0 = 4, kWarpSoftmax0 = 8;
 constexpr int kSenderThreads = 128;   // warps 4..7
-constexpr int kWgThreads = 128;       // one softmax warpgroup: warps 8..11 (even tiles), 12..15 (odd)
+constexpr int kWgThreads = 128;       // one softmax warpgroup: warps 8..11, 12..15
 constexpr int kSoftmaxThreads = 256;
 // Registers per thread: the launch gives every thread kLaunchRegs; the control warpgroup
 // (warps 0..3) drops to ctrl, the sender warpgroup to sender, and the two softmax
 // warpgroups rise to softmax.  The sum must not exceed 512 * kLaunchRegs (65,536); the split
 // follows each cache format's register needs (FP8 tiles are decoded by the senders, NVFP4
-// tiles by the softmax warpgroups).
+// tiles by the softmax warpgroups) and is one for which ptxas spills nothing.
 constexpr uint32_t kLaunchRegs = 128;
 template <int KV>
 struct RegSplit;
@@ -123,11 +125,11 @@ struct RegSplit<MLA_KV_BF16> {
 };
 template <>
 struct RegSplit<MLA_KV_FP8_E4M3> {
-  static constexpr uint32_t ctrl = 80, sender = 128, softmax = 152;
+  static constexpr uint32_t ctrl = 88, sender = 128, softmax = 144;
 };
 template <>
 struct RegSplit<MLA_KV_NVFP4> {
-  static constexpr uint32_t ctrl = 64, sender = 96, softmax = 176;
+  static constexpr uint32_t ctrl = 72, sender = 128, softmax = 152;
 };
 template <int KV>
 constexpr bool reg_split_fits() {
@@ -182,7 +184,10 @@ struct Smem {
   uint8_t ostage[8][2048];
   uint8_t q_rope[kQRopeBytes];
   Bars bars;
-  unsigned long long mchain[128];  // per row: (tile index + 1) << 32 | reference max bits
+  union {
+    unsigned long long mchain[128];  // alternate tiles, per row: (tile index + 1) << 32 | reference max bits
+    float mx[2][2][128];             // both warpgroups per tile: [tile & 1][warpgroup][row] half-row maxima
+  };
   int4 items[kItemRing];           // work items {u, tok_lo, tok_hi, slot}; tok_hi < 0 ends the list
   int items_min[kItemRing];        // the item's unit's first attended position (sliding window)
   float ep_m[2][2][128];           // [item parity][warpgroup][row] reference max
@@ -312,23 +317,26 @@ __device__ __forceinline__ int item_take(const int4* ring, const int* ring_min, 
 
 // Quantized caches: decodes the raw FP8 / NVFP4 bytes of landed tile k in place into f16, in
 // the swizzled layouts the score and P.V MMAs read (rows that are not visible become zeros),
-// then releases the tile to the score MMAs.  Called by the 128 threads of one warpgroup
-// (tq = 0..127: row tq / 2, half-row tq & 1 = 18 chunks of 8 values); `bar_id` is that
-// warpgroup's named barrier, which separates every read of raw bytes from the in-place writes.
-template <int KV>
+// then releases the tile to the score MMAs.  Called by NT threads (128: one warpgroup, 256:
+// both softmax warpgroups; tq = 0..NT-1: row tq / (NT / 64), part tq % (NT / 64) of the row's
+// 36 chunks of 8 values); `bar_id` is those threads' named barrier, which separates every
+// read of raw bytes from the in-place writes.
+template <int KV, int NT>
 __device__ __forceinline__ bool prepare_tile(Smem& S, const DecodeParams& p, int k, int tq, uint32_t cr,
                                              uint32_t b_kv_full, uint32_t b_kv_ready, uint32_t bar_id,
                                              volatile int* abort_flag) {
+  constexpr int kParts = NT / kTileN, kCh = 36 / kParts;  // threads per row, chunks per thread
+  static_assert(kParts * kTileN == NT && kCh * kParts == 36, "thread count must split the tile's rows evenly");
   const int st = k % kStages;
   if (!ptx::mbar_wait(b_kv_full + 8 * st, (k / kStages) & 1, abort_flag)) return false;
-  const int pr = tq >> 1, phf = tq & 1;
+  const int pr = tq / kParts, phf = tq % kParts;
   uint8_t* base = S.stage[st];
   const bool valid = (S.tmask[st] >> pr) & 1ull;
-  uint32_t raw[18][2];
+  uint32_t raw[kCh][2];
   if (valid) {
 #pragma unroll
-    for (int i = 0; i < 18; ++i) {
-      const int c = 18 * phf + i;
+    for (int i = 0; i < kCh; ++i) {
+      const int c = kCh * phf + i;
       if (KV == MLA_KV_FP8_E4M3) {
         const uint2 v = *reinterpret_cast<const uint2*>(c < 32 ? base + kRawFp8 + pr * 256 + 8 * c
                                                                : base + kRawFp8Rope + pr * 32 + 8 * (c - 32));
@@ -344,9 +352,9 @@ __device__ __forceinline__ bool prepare_tile(Smem& S, const DecodeParams& p, int
       }
     }
   }
-  ptx::named_bar_sync(bar_id, 128);  // every raw byte of the tile is in registers
+  ptx::named_bar_sync(bar_id, NT);  // every raw byte of the tile is in registers
 #pragma unroll
-  for (int i = 0; i < 18; ++i) {
+  for (int i = 0; i < kCh; ++i) {
     uint4 o = make_uint4(0u, 0u, 0u, 0u);
     if (valid) {
       if (KV == MLA_KV_FP8_E4M3) {
@@ -364,7 +372,7 @@ __device__ __forceinline__ bool prepare_tile(Smem& S, const DecodeParams& p, int
     }
     // chunk c (8 values) of row pr: latent chunks in the 128-byte swizzle of their 64-column
     // box, rope chunks in the 64-byte swizzle
-    const int c = 18 * phf + i;
+    const int c = kCh * phf + i;
     *reinterpret_cast<uint4*>(c < 32 ? base + (c >> 3) * kLatBox + pr * 128 + (((c & 7) ^ (pr & 7)) * 16)
                                      : base + 4 * kLatBox + pr * 64 + ((((c - 32) ^ ((pr >> 1) & 3))) * 16)) = o;
   }
@@ -372,17 +380,25 @@ __device__ __forceinline__ bool prepare_tile(Smem& S, const DecodeParams& p, int
   ptx::mbar_arrive(b_kv_ready + 8 * st);
   return true;
 }
-// Which warpgroup decodes a quantized cache: the senders (FP8: light decoding, done before
-// sending the previous tile's scores) or each softmax warpgroup for its own next tile (NVFP4:
-// heavier decoding, which would otherwise hold the senders back).
+// How the softmax warpgroups share the tiles, who decodes a quantized cache and who pushes a
+// tile's partial scores to the peer CTA (each choice measured on one box against the others):
+//   bf16   both warpgroups take every tile, 32 columns each (each tile's softmax, which sits
+//          on the cycle slot -> peer's push -> softmax -> P.V -> slot, then takes about half
+//          as long as one warpgroup taking all 64 columns of alternate tiles: 71.7 -> 67.6 us
+//          on 32 x 4096 tokens); the senders push.
+//   FP8    alternate tiles, all 64 columns: the senders decode every tile as it lands, and
+//          each softmax warpgroup pushes its own tile's scores, so that a push never waits
+//          behind a decode or behind the other tile's softmax (417 us on 128 x 8192 tokens,
+//          against 500-614 us for the other arrangements).
+//   NVFP4  both warpgroups take every tile and decode the tiles together, two ahead of the
+//          one whose softmax runs (its heavier decoding would hold the senders' pushes back);
+//          the senders push.
+template <int KV>
+constexpr bool half_tiles() { return KV != MLA_KV_FP8_E4M3; }
 template <int KV>
 constexpr bool decode_in_softmax() { return KV == MLA_KV_NVFP4; }
 template <int KV>
 constexpr bool decode_in_senders() { return KV == MLA_KV_FP8_E4M3; }
-// Who pushes a tile's partial scores to the peer CTA.  FP8: the tile's softmax warpgroup,
-// straight from the scores it has just read, so that the senders, which decode every tile,
-// never hold a send back behind a tile still in flight (A/B on one box: 472 -> 417 us on the
-// FP8 workload).  bf16 / NVFP4: the senders, which otherwise only load Q (3-4 % faster there).
 template <int KV>
 constexpr bool send_in_softmax() { return KV == MLA_KV_FP8_E4M3; }
 
@@ -423,13 +439,13 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
     S.status = 0u;
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(b_kv_full + 8 * s, 1);
-      ptx::mbar_init(b_kv_ready + 8 * s, KV == MLA_KV_BF16 ? 1 : kWgThreads);
+      ptx::mbar_init(b_kv_ready + 8 * s, KV == MLA_KV_BF16 ? 1 : decode_in_softmax<KV>() ? kSoftmaxThreads : kSenderThreads);
       ptx::mbar_init(b_kv_empty + 8 * s, 1);
     }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(b_s_full + 8 * s, 1);
-      ptx::mbar_init(b_s_free + 8 * s, kWgThreads + (send_in_softmax<KV>() ? 0 : kSenderThreads));
-      ptx::mbar_init(b_p_full + 8 * s, kWgThreads);
+      ptx::mbar_init(b_s_free + 8 * s, (half_tiles<KV>() ? kSoftmaxThreads : kWgThreads) + (send_in_softmax<KV>() ? 0 : kSenderThreads));
+      ptx::mbar_init(b_p_full + 8 * s, half_tiles<KV>() ? kSoftmaxThreads : kWgThreads);
       ptx::mbar_init(b_x_full + 8 * s, 1);   // one local arrive (expect_tx) + 24 KB of peer bytes
       ptx::mbar_init(b_x_empty + 8 * s, 1);  // one arrive per use, from the peer's P.V commit
     }
@@ -448,7 +464,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
     S.abort_flag = 0;
     ptx::fence_mbar_init_cluster();
   }
-  if (tid < 128) S.mchain[tid] = 0ull;
+  if (!half_tiles<KV>() && tid < 128) S.mchain[tid] = 0ull;
   if (warp == kWarpMma) {
     ptx::tmem_alloc(ptx::smem_u32(&S.tmem_base), kTmemCols);
     ptx::tmem_relinquish();
@@ -834,7 +850,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
         }
         if (decode_in_senders<KV>()) {
           for (int t = 0; t < nt; ++t)
-            if (!prepare_tile<KV>(S, p, g + t, tq, cr, b_kv_full, b_kv_ready, 3, abort_flag)) {
+            if (!prepare_tile<KV, kSenderThreads>(S, p, g + t, tq, cr, b_kv_full, b_kv_ready, 3, abort_flag)) {
               dead = true;
               break;
             }
@@ -863,7 +879,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
             dead = true;
             break;
           }
-          if (decode_in_senders<KV>() && !prepare_tile<KV>(S, p, g, tq, cr, b_kv_full, b_kv_ready, 3, abort_flag)) {
+          if (decode_in_senders<KV>() && !prepare_tile<KV, kSenderThreads>(S, p, g, tq, cr, b_kv_full, b_kv_ready, 3, abort_flag)) {
             dead = true;
             break;
           }
@@ -883,21 +899,27 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
   } else if (warp >= kWarpSoftmax0) {
     // ------------------------------------------------------------------ softmax + epilogue
     regs_to<RegSplit<KV>::softmax>();
+    // kHalf: both warpgroups take every tile, 32 of its 64 columns each; otherwise the two
+    // warpgroups take alternate tiles (even / odd), all 64 columns.
+    constexpr bool kHalf = half_tiles<KV>();
+    constexpr int kCols = kHalf ? 32 : 64;            // tile columns per thread
+    constexpr int kGroups = kCols * kXGroups / 64;    // their 16-byte groups in an exchange slot
+    constexpr int kStep = kHalf ? 1 : 2;
+    static_assert(kHalf || !decode_in_softmax<KV>(), "softmax decoding is written for both warpgroups per tile");
+    static_assert(!kHalf || !send_in_softmax<KV>(), "softmax pushes are written for alternate tiles");
     const int sw = warp - kWarpSoftmax0;        // 0..7
-    const int wg = sw >> 2;                      // tiles g with g & 1 == wg; O columns [128 wg, +128)
+    const int wg = sw >> 2;                      // O columns [128 wg, +128) in the epilogue
     const int q = warp & 3;                       // TMEM lane quadrant this warp may access
     const int row = 32 * q + lane;                // head
+    const int ts = 128 * wg + row;                // 0..255 over both warpgroups
+    const int c0 = kHalf ? 32 * wg : 0;           // this thread's first tile column
     const uint32_t lane_off = (uint32_t)(32 * q) << 16;
-    const uint32_t t_s = tmem + lane_off + kTmemS + 64 * wg;
+    const uint32_t t_s0 = tmem + lane_off + kTmemS + c0;
     const uint32_t t_o = tmem + lane_off + kTmemO;
     const float scale_log2 = p.sm_scale * p.kv_scale * kLog2e;
-    const uint32_t b_pf = b_p_full + 8 * wg, b_xf = b_x_full + 8 * wg, b_sf = b_s_full + 8 * wg;
-    const uint32_t b_sfree = b_s_free + 8 * wg;
-    // this warpgroup sends its tiles' partial scores into the peer's slot wg
-    const uint32_t x_peer = ptx::mapa(ptx::smem_u32(&S.xbuf[wg][0][0]), peer) + (uint32_t)row * 16;
-    const uint32_t bx_full_peer = ptx::mapa(b_x_full + 8 * wg, peer);
-    const uint32_t b_xe = b_x_empty + 8 * wg;
-    uint8_t* const pslot = reinterpret_cast<uint8_t*>(&S.xbuf[wg][0][0]);
+    // FP8: a warpgroup pushes its tiles' partial scores into the peer's slot g&1 itself
+    const uint32_t x_peer = ptx::mapa(ptx::smem_u32(&S.xbuf[0][0][0]), peer) + (uint32_t)row * 16;
+    const uint32_t bx_full_peer = ptx::mapa(b_x_full, peer);
     unsigned long long* const chain = &S.mchain[row];
 
     // P.V completions: o_done[k & 3] completes once per P.V(k), k = j, j + 4, ...  Every P.V
@@ -921,19 +943,21 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       const int b = it.u / p.q_len;
       const int nt = (it.tok_hi - it.tok_lo + kTileN - 1) / kTileN;
       const int g0 = g;
-      float m_own = -INFINITY, l_own = 0.f;  // this warpgroup's row sum and the reference it is relative to
-      int t_idx = (g0 & 1) == wg ? 0 : 1;     // this warpgroup's first tile of the item
-      // The first item starts with one pass through the loop body that has no effect (every
-      // wait, arrive and store is skipped): it fetches the body's instructions while the
-      // first scores are still being computed, instead of on the first tile's critical path.
-      if (k_item == 0) t_idx -= 2;
-      // quantized caches: this warpgroup decodes the tiles it will take (each one as soon as
-      // it has handed over the previous one's P; on the first item, at the end of the
-      // instruction-fetch pass)
-      if (decode_in_softmax<KV>() && k_item > 0 && t_idx < nt &&
-          !prepare_tile<KV>(S, p, g0 + t_idx, 32 * q + lane, cr, b_kv_full, b_kv_ready, 4 + wg, abort_flag)) {
-        dead = true;
-        break;
+      // the row's reference and this thread's running sum relative to it
+      float m_own = -INFINITY, l_own = 0.f;
+      int t_idx = kHalf || (g0 & 1) == wg ? 0 : 1;  // this thread's first tile of the item
+      // The first item starts with passes through the loop body that have no effect (every
+      // wait, arrive and store is skipped): they fetch the body's instructions while the
+      // first scores are still being computed, instead of on the first tile's critical path
+      // (NVFP4: two passes, whose ends decode the item's first two tiles).
+      if (k_item == 0) t_idx -= kHalf ? (decode_in_softmax<KV>() ? 2 : 1) : 2;
+      // NVFP4: tiles are decoded two ahead of the one whose softmax is running, by both
+      // warpgroups together; an item's first two here (the first item's: at the ends of the
+      // instruction-fetch passes)
+      if (decode_in_softmax<KV>() && k_item > 0) {
+        for (int t = 0; t < nt && t < 2 && !dead; ++t)
+          if (!prepare_tile<KV, kSoftmaxThreads>(S, p, g0 + t, ts, cr, b_kv_full, b_kv_ready, 4, abort_flag)) dead = true;
+        if (dead) break;
       }
       // quantized caches: the exponent this CTA's half of the item's q row was scaled by
       float q_sc = 1.f;
@@ -948,76 +972,71 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
         q_sc = pow2f(e);
         q_scaled = __any_sync(0xffffffffu, e != 0);
       }
-      for (; t_idx < nt; t_idx += 2) {
+      for (; t_idx < nt; t_idx += kStep) {
         const bool real = t_idx >= 0;
         const int gg = g0 + t_idx;
+        const int slot = gg & 1;
         // ---- own partial scores
-        float s[64];
-        if (real && !ptx::mbar_wait(b_sf, (gg >> 1) & 1, abort_flag)) { dead = true; break; }
+        float s[kCols];
+        if (real && !ptx::mbar_wait(b_s_full + 8 * slot, (gg >> 1) & 1, abort_flag)) { dead = true; break; }
         ptx::tc_fence_after();
         {
-          uint32_t r0[32], r1[32];
-          ptx::tmem_ld32(t_s, r0);
-          ptx::tmem_ld32(t_s + 32, r1);
+          uint32_t r[kCols / 32][32];
+#pragma unroll
+          for (int h = 0; h < kCols / 32; ++h) ptx::tmem_ld32(t_s0 + 64 * slot + 32 * h, r[h]);
           ptx::tmem_ld_wait();
           ptx::tc_fence_before();
-          if (real) ptx::mbar_arrive(b_sfree);
+          if (real) ptx::mbar_arrive(b_s_free + 8 * slot);
           if (KV != MLA_KV_BF16 && q_scaled) {  // back to the scale of the unscaled row (exact)
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-              r0[k] = __float_as_uint(__uint_as_float(r0[k]) * q_sc);
-              r1[k] = __float_as_uint(__uint_as_float(r1[k]) * q_sc);
-            }
+            for (int k = 0; k < kCols; ++k) r[k >> 5][k & 31] = __float_as_uint(__uint_as_float(r[k >> 5][k & 31]) * q_sc);
           }
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            s[k] = __uint_as_float(r0[k]);
-            s[32 + k] = __uint_as_float(r1[k]);
-          }
-          // ---- this tile's partial scores -> the peer: 16 values -> 12 packed words -> three
-          // 16-byte stores, four times; the slot is free once the peer's P.V of this
+          for (int k = 0; k < kCols; ++k) s[k] = __uint_as_float(r[k >> 5][k & 31]);
+          // ---- FP8: this tile's partial scores -> the peer: 16 values -> 12 packed words ->
+          // three 16-byte stores, four times; the slot is free once the peer's P.V of this
           // warpgroup's previous tile has read it
           if (send_in_softmax<KV>() && real) {
             const int use = gg >> 1;
-            if (use >= 1 && !ptx::mbar_wait(b_xe, (use - 1) & 1, abort_flag, true)) {
+            if (use >= 1 && !ptx::mbar_wait(b_x_empty + 8 * slot, (use - 1) & 1, abort_flag, true)) {
               dead = true;
             } else {
 #pragma unroll
-              for (int h = 0; h < 4; ++h) {
-                const uint32_t* src = h < 2 ? r0 + 16 * h : r1 + 16 * (h - 2);
+              for (int h = 0; h < kCols / 16; ++h) {
                 uint32_t pw[12];
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                  pack24x4(src[4 * j], src[4 * j + 1], src[4 * j + 2], src[4 * j + 3], pw[3 * j], pw[3 * j + 1],
-                           pw[3 * j + 2]);
+                for (int j = 0; j < 4; ++j) {
+                  const uint32_t* v = &r[h >> 1][16 * (h & 1) + 4 * j];
+                  pack24x4(v[0], v[1], v[2], v[3], pw[3 * j], pw[3 * j + 1], pw[3 * j + 2]);
+                }
 #pragma unroll
                 for (int j = 0; j < 3; ++j)
-                  ptx::st_async_v4(x_peer + (3 * h + j) * 128 * 16, __uint_as_float(pw[4 * j]),
+                  ptx::st_async_v4(x_peer + (uint32_t)slot * kXBytes + (3 * h + j) * 128 * 16, __uint_as_float(pw[4 * j]),
                                    __uint_as_float(pw[4 * j + 1]), __uint_as_float(pw[4 * j + 2]),
-                                   __uint_as_float(pw[4 * j + 3]), bx_full_peer);
+                                   __uint_as_float(pw[4 * j + 3]), bx_full_peer + 8 * slot);
               }
             }
           }
         }
         if (dead) break;
-        // ---- the peer's partial scores (pushed by its senders)
-        if (real && q == 0 && lane == 0) ptx::mbar_arrive_expect_tx(b_xf, kXBytes);
-        if (real && !ptx::mbar_wait(b_xf, (gg >> 1) & 1, abort_flag, true)) { dead = true; break; }
+        // ---- the peer's partial scores of this thread's columns
+        if (real && (kHalf ? ts : row) == 0) ptx::mbar_arrive_expect_tx(b_x_full + 8 * slot, kXBytes);
+        if (real && !ptx::mbar_wait(b_x_full + 8 * slot, (gg >> 1) & 1, abort_flag, true)) { dead = true; break; }
         // the peer pushed these only after P.V(gg-2) of this CTA had read the slot
         if (real && gg - 2 > pv_known) pv_known = gg - 2;
-        uint32_t xw[48];
+        uint32_t xw[4 * kGroups];
 #pragma unroll
-        for (int k = 0; k < kXGroups; ++k) {
-          const uint4 v = S.xbuf[wg][k][row];
+        for (int k = 0; k < kGroups; ++k) {
+          const uint4 v = S.xbuf[slot][c0 / 16 * 3 + k][row];
           xw[4 * k] = v.x;
           xw[4 * k + 1] = v.y;
           xw[4 * k + 2] = v.z;
           xw[4 * k + 3] = v.w;
         }
-        // every row of the slot has been read: P may overwrite it
-        ptx::named_bar_sync(1 + wg, kWgThreads);
+        // alternate tiles: every row of the slot has been read, P may overwrite it
+        if constexpr (!kHalf) ptx::named_bar_sync(1 + wg, kWgThreads);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
+        for (int j = 0; j < kCols / 4; ++j) {
           float a, b2, c, d;
           unpack24x4(xw[3 * j], xw[3 * j + 1], xw[3 * j + 2], a, b2, c, d);
           s[4 * j] += a;
@@ -1025,47 +1044,61 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
           s[4 * j + 2] += c;
           s[4 * j + 3] += d;
         }
-        // ---- mask (tail tiles only), row max (raw units; the scale is positive)
-        // the producer published the tile's row mask with the tile's kv_full phase, which
-        // completed before this tile's scores (and cannot move on before P(gg) is handed over)
+        // ---- mask (tail tiles only), row max over this thread's columns (raw units; the
+        // scale is positive).  The producer published the tile's row mask with the tile's
+        // kv_full phase, which completed before this tile's scores (and cannot move on before
+        // P(gg) is handed over).
         const int st = real ? gg % kStages : 0;
         if (real && !ptx::mbar_wait(b_kv_full + 8 * st, (gg / kStages) & 1, abort_flag)) { dead = true; break; }
-        const uint64_t mask = S.tmask[st];
-        if (mask != ~0ull) {
+        const uint64_t full = kCols == 64 ? ~0ull : (1ull << kCols) - 1;
+        const uint64_t mask = (S.tmask[st] >> c0) & full;
+        if (mask != full) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) s[c] = ((mask >> c) & 1ull) ? s[c] : -INFINITY;
+          for (int c = 0; c < kCols; ++c) s[c] = ((mask >> c) & 1ull) ? s[c] : -INFINITY;
         }
         float m4[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-        for (int c = 4; c < 64; c += 4) {
+        for (int c = 4; c < kCols; c += 4) {
           m4[0] = fmaxf(m4[0], s[c]);
           m4[1] = fmaxf(m4[1], s[c + 1]);
           m4[2] = fmaxf(m4[2], s[c + 2]);
           m4[3] = fmaxf(m4[3], s[c + 3]);
         }
-        const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * scale_log2;
-        // ---- reference max: take the previous tile's, move it when this tile exceeds it by > 8
+        float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        if constexpr (kHalf) {
+          // the two halves of the row meet: every row of the slot has been read (P may
+          // overwrite it), and each half takes the other's maximum
+          S.mx[slot][wg][row] = mt;
+          ptx::named_bar_sync(1, kSoftmaxThreads);
+          mt = fmaxf(S.mx[slot][0][row], S.mx[slot][1][row]);
+        }
+        mt *= scale_log2;
+        // ---- reference max: kept from tile to tile, moved when a tile exceeds it by > 8
+        // (both halves of a row take the same decision; alternate tiles pass it from one
+        // warpgroup to the other through shared memory)
         float m_prev = -INFINITY;
-        if (gg > 0) {
+        if constexpr (kHalf) {
+          if (t_idx > 0) m_prev = m_own;
+        } else if (gg > 0) {
           unsigned long long v;
           if (!chain_wait(chain, (unsigned)gg, v, abort_flag)) { dead = true; break; }
           if (t_idx > 0) m_prev = __uint_as_float((uint32_t)v);
         }
         const bool grow = mt > m_prev + kRescaleThreshold;
         const float m_new = grow ? mt : m_prev;
-        if (real)
+        if (!kHalf && real)
           *reinterpret_cast<volatile unsigned long long*>(chain) =
               ((unsigned long long)(unsigned)(gg + 1) << 32) | __float_as_uint(m_new);
-        // this warpgroup's running sum follows the reference
+        // this thread's running sum follows the reference
         if (real && m_new != m_own) {
           if (l_own != 0.f) l_own *= ptx::ex2_approx(m_own - m_new);
           m_own = m_new;
         }
         const float m_use = m_new == -INFINITY ? 0.f : m_new;
-        uint32_t pk[32];
+        uint32_t pk[kCols / 2];
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
+        for (int c = 0; c < kCols; c += 2) {
           const float p0 = ptx::ex2_approx(fmaf(s[c], scale_log2, -m_use));
           const float p1 = ptx::ex2_approx(fmaf(s[c + 1], scale_log2, -m_use));
           ls[(c >> 1) & 3] += p0 + p1;
@@ -1077,34 +1110,37 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
         // P(gg) -> the slot.  Row r, 16-byte chunk c (8 tokens) sits at chunk position
         // c ^ (r & 7) of the row's 128 bytes (the 128-byte swizzle the P.V MMAs read).
         if (real) {
+          uint8_t* const prow = reinterpret_cast<uint8_t*>(&S.xbuf[slot][0][0]) + row * 128;
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(pslot + row * 128 + ((c ^ (row & 7)) * 16)) =
+          for (int c = 0; c < kCols / 8; ++c)
+            *reinterpret_cast<uint4*>(prow + (((c0 / 8 + c) ^ (row & 7)) * 16)) =
                 make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
         }
         if (t_idx > 0 && __any_sync(0xffffffffu, grow)) {
-          // O (all 256 columns of these rows) moves to the new reference once P.V(gg-1) is
-          // done, before P(gg) is handed over
+          // O moves to the new reference once P.V(gg-1) is done, before P(gg) is handed
+          // over: this half's 128 columns, or all 256 (alternate tiles)
           if (!wait_pv(gg - 1)) { dead = true; break; }
           ptx::tc_fence_after();
           const float a = grow ? ptx::ex2_approx(m_prev - m_new) : 1.f;
+          constexpr int kOChunks = kHalf ? 8 : 16;
+          const uint32_t t_oc = t_o + (kHalf ? 128 * wg : 0);
 #pragma unroll 1
-          for (int c = 0; c < 16; ++c) {
+          for (int c = 0; c < kOChunks; ++c) {
             uint32_t r[16];
-            ptx::tmem_ld16(t_o + 16 * c, r);
+            ptx::tmem_ld16(t_oc + 16 * c, r);
             ptx::tmem_ld_wait();
 #pragma unroll
             for (int k = 0; k < 16; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * a);
-            ptx::tmem_st16(t_o + 16 * c, r);
+            ptx::tmem_st16(t_oc + 16 * c, r);
           }
           ptx::tmem_st_wait();
         }
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
-        if (real) ptx::mbar_arrive(b_pf);
-        // quantized caches: decode this warpgroup's next tile of the item now
+        if (real) ptx::mbar_arrive(b_p_full + 8 * slot);
+        // NVFP4: decode the item's tile two ahead now
         if (decode_in_softmax<KV>() && t_idx + 2 < nt &&
-            !prepare_tile<KV>(S, p, gg + 2, 32 * q + lane, cr, b_kv_full, b_kv_ready, 4 + wg, abort_flag)) {
+            !prepare_tile<KV, kSoftmaxThreads>(S, p, gg + 2, ts, cr, b_kv_full, b_kv_ready, 4, abort_flag)) {
           dead = true;
           break;
         }
@@ -1218,11 +1254,11 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       ptx::mbar_arrive(b_o_free);
       ++n_item;
     }
-    // the peer's P.V commit for this warpgroup's last tile lands on x_empty[wg]: take it
+    // FP8: the peer's P.V commit for this warpgroup's last tile lands on x_empty[wg]: take it
     // before exit
     if (send_in_softmax<KV>() && !dead && g > 0) {
       const int last = ((g - 1) & 1) == wg ? g - 1 : g - 2;
-      if (last >= 0) ptx::mbar_wait(b_xe, (uint32_t)(last >> 1) & 1u, abort_flag, true);
+      if (last >= 0) ptx::mbar_wait(b_x_empty + 8 * wg, (uint32_t)(last >> 1) & 1u, abort_flag, true);
     }
   } else if (warp == kWarpItems) {
     // ------------------------------------------------------------------ work items
