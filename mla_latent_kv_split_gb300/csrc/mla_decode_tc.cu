@@ -105,6 +105,9 @@ constexpr int kItemRing = 16;
 // item k-4 has been read.
 constexpr int kQExpRing = 4;
 constexpr uint32_t kItemReaders = 15;
+// All query rows are asked into L2 at the start (each CTA a share) when they total at most
+// this many bytes; otherwise each item's rows are asked for one item ahead.
+constexpr size_t kQPrefetchBytes = 64u << 20;
 
 // warp roles
 constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpMmaPv = 2, kWarpItems = 3, kWarpSender0 = 4, kWarpSoftmax0 = 8;
@@ -129,7 +132,7 @@ struct RegSplit<MLA_KV_FP8_E4M3> {
 };
 template <>
 struct RegSplit<MLA_KV_NVFP4> {
-  static constexpr uint32_t ctrl = 72, sender = 128, softmax = 152;
+  static constexpr uint32_t ctrl = 88, sender = 128, softmax = 144;
 };
 template <int KV>
 constexpr bool reg_split_fits() {
@@ -197,10 +200,9 @@ struct Smem {
   uint32_t tmem_base;
   int abort_flag;
   unsigned status;  // this CTA's status bits
-  int scratch[33];
-  WorkerStart wstart;  // this worker's place in the schedule (the full plan is built in xbuf)
+  WorkerStart wstart;  // this worker's place in the schedule (the full plan is built in stage 0)
 };
-static_assert(sizeof(PlanSmem) <= 2 * kXBytes, "plan scratch must fit the exchange buffers");
+static_assert(sizeof(PlanSmem) <= kStageBytes, "plan scratch must fit one cache stage");
 static_assert(kXBytes % 1024 == 0 && (kStages * kStageBytes) % 1024 == 0, "P tiles need 1024-byte alignment");
 
 __device__ __forceinline__ Smem& smem_ref(uint8_t* raw) {
@@ -462,6 +464,9 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       ptx::mbar_init(b_item_empty + 8 * s, kItemReaders);
     }
     S.abort_flag = 0;
+    // each exchange slot's first use is armed here, every later one as soon as the
+    // previous use has completed
+    for (int s = 0; s < 2; ++s) ptx::mbar_arrive_expect_tx(b_x_full + 8 * s, kXBytes);
     ptx::fence_mbar_init_cluster();
   }
   if (!half_tiles<KV>() && tid < 128) S.mchain[tid] = 0ull;
@@ -473,30 +478,48 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
     ptx::prefetch_tmap(&tm_lat);
     ptx::prefetch_tmap(&tm_rope);
   }
-  if (warp == kWarpMmaPv && lane == 0) {
-    const size_t table = (size_t)p.B * p.max_pages * 4 & ~(size_t)15;
-    const size_t share = (((table + gridDim.x - 1) / gridDim.x) + 15) & ~(size_t)15;
+  // this CTA's share of an array, on its way to L2
+  auto prefetch_share = [&](const void* base, size_t bytes) {
+    bytes &= ~(size_t)15;
+    const size_t share = (((bytes + gridDim.x - 1) / gridDim.x) + 15) & ~(size_t)15;
     const size_t lo = (size_t)blockIdx.x * share;
-    if (lo < table)
-      ptx::bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(p.block_table) + lo, (uint32_t)min(share, table - lo));
+    if (lo < bytes) ptx::bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(base) + lo, (uint32_t)min(share, bytes - lo));
+  };
+  const size_t q_rows = (size_t)p.B * p.q_len * p.H;
+  const bool q_share = q_rows * (kLatent + kRope) * 2 <= kQPrefetchBytes;
+  if (warp == kWarpMmaPv && lane == 0) prefetch_share(p.block_table, (size_t)p.B * p.max_pages * 4);
+  if (warp == kWarpItems && lane == 0 && q_share) {
+    prefetch_share(p.q_nope, q_rows * kLatent * 2);
+    prefetch_share(p.q_pe, q_rows * kRope * 2);
   }
-  __syncthreads();
-  {
-    // the schedule is evaluated in the exchange buffers, which are idle until the first tile
-    PlanSmem& plan = *reinterpret_cast<PlanSmem*>(&S.xbuf[0][0][0]);
-    compute_plan(p, plan, S.scratch, &S.status, blockIdx.x == 0);
-    if (tid == 0) {
+  // From here on the peer may address this CTA's barriers and exchange buffers.
+  ptx::cluster_arrive();
+  // One warp evaluates the schedule, in the first cache stage (idle until the first tile is
+  // loaded, which happens after this), and finds this worker's start; the other warps go on
+  // to the barrier below.
+  if (warp == kWarpProducer) {
+    __syncwarp();
+    PlanSmem& plan = *reinterpret_cast<PlanSmem*>(S.stage[0]);
+    compute_plan_warp(p, plan, &S.status, blockIdx.x == 0);
+    if (lane == 0) {
       S.wstart = worker_start(p, plan, worker);
       // the first item's query rows, on their way to L2 before the roles start
-      if (S.wstart.busy && cr == 0) {
+      if (S.wstart.busy && cr == 0 && !q_share) {
         ptx::bulk_prefetch_l2(p.q_nope + (size_t)S.wstart.u0 * p.H * kLatent, (uint32_t)p.H * kLatent * 2);
         ptx::bulk_prefetch_l2(p.q_pe + (size_t)S.wstart.u0 * p.H * kRope, (uint32_t)p.H * kRope * 2);
+      }
+      // the block-table entries of the first tile, into L1 for the producer
+      const WorkItem& f = S.wstart.first;
+      if (S.wstart.busy) {
+        const int* row = p.block_table + (size_t)(f.u / p.q_len) * p.max_pages + (f.tok_lo >> (p.page_size == 32 ? 5 : 6));
+        ptx::prefetch_l1(row);
+        if (p.page_size == 32 && f.tok_lo + 32 < f.tok_hi) ptx::prefetch_l1(row + 1);
       }
     }
   }
   ptx::tc_fence_before();
   __syncthreads();
-  ptx::cluster_sync_all();  // the peer's barriers exist before any remote arrive
+  ptx::cluster_wait();  // the peer's barriers exist before any remote arrive
   ptx::tc_fence_after();
   const WorkerStart& wst = S.wstart;  // read from shared memory where needed
   const int n_tiles_total = wst.N;
@@ -515,11 +538,24 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
     int g = 0;
     bool dead = false;
     WorkItem it;
+    // The first item comes from the schedule evaluated at start-up (its first tile's
+    // block-table entries already asked into L1); its ring entry is taken together with the
+    // second.
+    const bool first_known = wst.busy != 0;
     for (int k_item = 0;; ++k_item) {
-      const int got = item_take(S.items, S.items_min, b_item_full, b_item_empty, k_item, abort_flag, it, true);
-      if (got <= 0) {
-        dead = got < 0;
-        break;
+      if (k_item == 0 && first_known) {
+        it = wst.first;
+      } else {
+        if (k_item == 1 && first_known &&
+            item_take(S.items, S.items_min, b_item_full, b_item_empty, 0, abort_flag, it, true) < 0) {
+          dead = true;
+          break;
+        }
+        const int got = item_take(S.items, S.items_min, b_item_full, b_item_empty, k_item, abort_flag, it, true);
+        if (got <= 0) {
+          dead = got < 0;
+          break;
+        }
       }
       const int b = it.u / p.q_len;
       TileInfo ti_next = tile_info(p, b, it.tok_lo, it.tok_hi, it.tok_min);
@@ -721,22 +757,43 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
         }
       }
       const int slot = k & 1, use = k >> 1;
-      // the peer's P.V(k-2) has read the slot (its P) before the next scores go in
-      if (use >= 1 && !ptx::mbar_wait(b_x_empty + 8 * slot, (use - 1) & 1, abort_flag, true)) return false;
       const uint32_t xp = x_peer + (uint32_t)slot * kXBytes + (uint32_t)row * 16;
       const uint32_t bar = bx_full_peer + 8 * slot;
-      // 16 values -> 12 packed words -> three 16-byte stores, four times
+      if constexpr (KV == MLA_KV_BF16) {
+        // the peer's P.V(k-2) has read the slot (its P) before the next scores go in
+        if (use >= 1 && !ptx::mbar_wait(b_x_empty + 8 * slot, (use - 1) & 1, abort_flag, true)) return false;
+        // 16 values -> 12 packed words -> three 16-byte stores, four times
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const uint32_t* src = h < 2 ? r0 + 16 * h : r1 + 16 * (h - 2);
-        uint32_t pw[12];
+        for (int h = 0; h < 4; ++h) {
+          const uint32_t* src = h < 2 ? r0 + 16 * h : r1 + 16 * (h - 2);
+          uint32_t pw[12];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          pack24x4(src[4 * j], src[4 * j + 1], src[4 * j + 2], src[4 * j + 3], pw[3 * j], pw[3 * j + 1], pw[3 * j + 2]);
+          for (int j = 0; j < 4; ++j)
+            pack24x4(src[4 * j], src[4 * j + 1], src[4 * j + 2], src[4 * j + 3], pw[3 * j], pw[3 * j + 1], pw[3 * j + 2]);
 #pragma unroll
-        for (int j = 0; j < 3; ++j)
-          ptx::st_async_v4(xp + (3 * h + j) * 128 * 16, __uint_as_float(pw[4 * j]), __uint_as_float(pw[4 * j + 1]),
-                           __uint_as_float(pw[4 * j + 2]), __uint_as_float(pw[4 * j + 3]), bar);
+          for (int j = 0; j < 3; ++j)
+            ptx::st_async_v4(xp + (3 * h + j) * 128 * 16, __uint_as_float(pw[4 * j]), __uint_as_float(pw[4 * j + 1]),
+                             __uint_as_float(pw[4 * j + 2]), __uint_as_float(pw[4 * j + 3]), bar);
+        }
+      } else {
+        // NVFP4 (whose sender budget is the tighter one): all 64 values packed first, which
+        // frees the score registers before the wait
+        uint32_t pw[4][12];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const uint32_t* src = h < 2 ? r0 + 16 * h : r1 + 16 * (h - 2);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            pack24x4(src[4 * j], src[4 * j + 1], src[4 * j + 2], src[4 * j + 3], pw[h][3 * j], pw[h][3 * j + 1],
+                     pw[h][3 * j + 2]);
+        }
+        if (use >= 1 && !ptx::mbar_wait(b_x_empty + 8 * slot, (use - 1) & 1, abort_flag, true)) return false;
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+#pragma unroll
+          for (int j = 0; j < 3; ++j)
+            ptx::st_async_v4(xp + (3 * h + j) * 128 * 16, __uint_as_float(pw[h][4 * j]), __uint_as_float(pw[h][4 * j + 1]),
+                             __uint_as_float(pw[h][4 * j + 2]), __uint_as_float(pw[h][4 * j + 3]), bar);
       }
       return true;
     };
@@ -1019,9 +1076,11 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
           }
         }
         if (dead) break;
-        // ---- the peer's partial scores of this thread's columns
-        if (real && (kHalf ? ts : row) == 0) ptx::mbar_arrive_expect_tx(b_x_full + 8 * slot, kXBytes);
+        // ---- the peer's partial scores of this thread's columns (then the slot's next use is
+        // armed: the peer pushes into it only after this tile's P.V, which every thread here
+        // reaches only after this wait)
         if (real && !ptx::mbar_wait(b_x_full + 8 * slot, (gg >> 1) & 1, abort_flag, true)) { dead = true; break; }
+        if (real && (kHalf ? ts : row) == 0) ptx::mbar_arrive_expect_tx(b_x_full + 8 * slot, kXBytes);
         // the peer pushed these only after P.V(gg-2) of this CTA had read the slot
         if (real && gg - 2 > pv_known) pv_known = gg - 2;
         uint32_t xw[4 * kGroups];

@@ -79,111 +79,77 @@ struct PlanSmem {
   int pref[kMaxUnits];       // exclusive prefix of the partial slots of split units
 };
 
-// Block-wide exclusive scan of vals[0..n) in place; returns the total.  All threads call.
-__device__ inline int block_exclusive_scan(int* vals, int n, int* scratch /*[33]*/) {
-  const int T = blockDim.x * blockDim.y * blockDim.z;
-  const int tid = threadIdx.x + blockDim.x * (threadIdx.y + blockDim.y * threadIdx.z);
-  const int per = (n + T - 1) / T;
-  const int lo = min(n, tid * per), hi = min(n, lo + per);
-  int local = 0;
-  for (int k = lo; k < hi; ++k) local += vals[k];
-  const int lane = tid & 31, warp = tid >> 5, nwarps = (T + 31) >> 5;
-  int incl = local;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, incl, d);
-    if (lane >= d) incl += y;
-  }
-  if (lane == 31) scratch[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < nwarps ? scratch[lane] : 0;
-    int wi = w;
+// Exclusive scan of vals[0..n) in place by one warp (all 32 lanes call); returns the total.
+__device__ inline int warp_exclusive_scan(int* vals, int n) {
+  const int lane = threadIdx.x & 31;
+  int carry = 0;
+  for (int base = 0; base < n; base += 32) {
+    const int k = base + lane;
+    const int v = k < n ? vals[k] : 0;
+    int x = v;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, wi, d);
-      if (lane >= d) wi += y;
+      const int y = __shfl_up_sync(0xffffffffu, x, d);
+      if (lane >= d) x += y;
     }
-    if (lane < nwarps) scratch[lane] = wi - w;  // exclusive warp offsets
-    if (lane == 31) scratch[32] = wi;           // total
+    if (k < n) vals[k] = carry + x - v;
+    carry += __shfl_sync(0xffffffffu, x, 31);
   }
-  __syncthreads();
-  int run = scratch[warp] + incl - local;
-  for (int k = lo; k < hi; ++k) {
-    int v = vals[k];
-    vals[k] = run;
-    run += v;
-  }
-  int total = scratch[32];
-  __syncthreads();
-  return total;
+  return carry;
 }
 
-// Evaluates the schedule in shared memory (all threads call).  Sets status bits for
-// malformed seq_lens.  When `write_plan` is set, also stores {parts, slot} per unit into
-// the workspace plan for the split-K reduce.
-__device__ inline void compute_plan(const DecodeParams& p, PlanSmem& pl, int* scratch, unsigned* cta_status,
-                                    bool write_plan) {
-  const int T = blockDim.x * blockDim.y * blockDim.z;
-  const int tid = threadIdx.x + blockDim.x * (threadIdx.y + blockDim.y * threadIdx.z);
+// Evaluates the schedule in shared memory with one warp (its 32 lanes call; no other thread
+// touches pl meanwhile).  Sets status bits for malformed seq_lens.  When `write_plan` is set,
+// also stores {parts, slot} per unit into the workspace plan for the split-K reduce.
+__device__ inline void compute_plan_warp(const DecodeParams& p, PlanSmem& pl, unsigned* cta_status, bool write_plan) {
+  const int lane = threadIdx.x & 31;
   const int U = p.B * p.q_len;
   unsigned bad = 0;
-  for (int k = tid; k < U; k += T) {
+  for (int k = lane; k < U; k += 32) {
     const int u = unit_at(k, p.B, p.q_len, p.num_splits);
-    int b = u / p.q_len, i = u % p.q_len;
-    int raw = __ldg(p.seq_lens + b);
+    const int b = u / p.q_len, i = u % p.q_len;
+    const int raw = __ldg(p.seq_lens + b);
     if (raw < 0) bad |= MLA_STATUS_NEG_SEQ_LEN;
     if ((long long)raw > (long long)p.max_pages * p.page_size) bad |= MLA_STATUS_SEQ_TOO_LONG;
-    int L = clamp_seq_len(raw, p.max_pages, p.page_size);
+    const int L = clamp_seq_len(raw, p.max_pages, p.page_size);
     if (L < p.q_len && i == 0) bad |= MLA_STATUS_SEQ_LT_QLEN;
-    int vis = unit_visible(L, p.q_len, i);
+    const int vis = unit_visible(L, p.q_len, i);
     pl.vis[k] = vis;
-    int tiles = unit_tiles(vis, p.window);
-    pl.begin[k] = p.num_splits > 0
-                      ? (tiles ? cdiv_i(tiles, forced_span_tiles(tiles, p.num_splits)) : 0)
-                      : unit_slots(tiles);
+    const int tiles = unit_tiles(vis, p.window);
+    pl.begin[k] = p.num_splits > 0 ? (tiles ? cdiv_i(tiles, forced_span_tiles(tiles, p.num_splits)) : 0)
+                                   : unit_slots(tiles);
   }
   if (bad && write_plan) set_status(cta_status, bad);
-  __syncthreads();
-  int N = block_exclusive_scan(pl.begin, U, scratch);
-  if (tid == 0) {
+  __syncwarp();
+  const int N = warp_exclusive_scan(pl.begin, U);
+  if (lane == 0) {
     pl.begin[U] = N;
     pl.N = N;
   }
-  __syncthreads();
-  // parts per unit -> slot scan (reuse pl.slot as the per-unit split-part count)
+  __syncwarp();
+  // parts per unit -> slot scan (pl.slot holds the per-unit split-part count first)
   const int Ca = active_workers(N, p.workers);
-  for (int k = tid; k < U; k += T) {
-    int parts;
-    if (p.num_splits > 0) {
-      parts = pl.begin[k + 1] - pl.begin[k];
-    } else {
-      // a unit's tiles are the last of its slots
-      parts = pl.begin[k + 1] > pl.begin[k]
-                  ? worker_of(pl.begin[k + 1] - 1, N, Ca) - worker_of(pl.begin[k] + kItemCost, N, Ca) + 1
-                  : 0;
-    }
+  auto parts_of = [&](int k) {
+    return p.num_splits > 0 ? pl.begin[k + 1] - pl.begin[k]
+         : (pl.begin[k + 1] > pl.begin[k]
+                ? worker_of(pl.begin[k + 1] - 1, N, Ca) - worker_of(pl.begin[k] + kItemCost, N, Ca) + 1
+                : 0);
+  };
+  int2* plan = reinterpret_cast<int2*>(p.ws + kPlanOffset);
+  for (int k = lane; k < U; k += 32) {
+    const int parts = parts_of(k);
     pl.slot[k] = parts > 1 ? parts : 0;
-    if (write_plan) {
-      int2* plan = reinterpret_cast<int2*>(p.ws + kPlanOffset);
-      plan[unit_at(k, p.B, p.q_len, p.num_splits)].x = parts;  // slot written below
-    }
+    if (write_plan) plan[unit_at(k, p.B, p.q_len, p.num_splits)].x = parts;
   }
-  __syncthreads();
-  block_exclusive_scan(pl.slot, U, scratch);
-  for (int k = tid; k < U; k += T) pl.pref[k] = pl.slot[k];
-  for (int k = tid; k < U; k += T) {
-    int parts = p.num_splits > 0 ? pl.begin[k + 1] - pl.begin[k]
-              : (pl.begin[k + 1] > pl.begin[k]
-                     ? worker_of(pl.begin[k + 1] - 1, N, Ca) - worker_of(pl.begin[k] + kItemCost, N, Ca) + 1
-                     : 0);
-    if (parts <= 1) pl.slot[k] = -1;
-    if (write_plan) {
-      int2* plan = reinterpret_cast<int2*>(p.ws + kPlanOffset);
-      plan[unit_at(k, p.B, p.q_len, p.num_splits)].y = pl.slot[k];
-    }
+  __syncwarp();
+  warp_exclusive_scan(pl.slot, U);
+  __syncwarp();
+  for (int k = lane; k < U; k += 32) {
+    pl.pref[k] = pl.slot[k];
+    if (parts_of(k) <= 1) pl.slot[k] = -1;
+    if (write_plan) plan[unit_at(k, p.B, p.q_len, p.num_splits)].y = pl.slot[k];
   }
-  __syncthreads();
+  __syncwarp();
 }
 
 // One work item: unit u, token range [tok_lo, tok_hi) of its visible KV, partial slot
