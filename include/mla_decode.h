@@ -36,8 +36,9 @@
  *     SM count and of the kernel attributes, and (mla_decode_no_alloc only) a per-device
  *     cache of its scratch buffer's address, each filled once under a lock, plus that
  *     scratch buffer itself: one per device, shared by every mla_decode_no_alloc call, so
- *     those calls must be ordered by the caller (see mla_decode_no_alloc).  Every other
- *     entry point touches only the caller's buffers.
+ *     those calls must be ordered by the caller (see mla_decode_no_alloc); and the
+ *     small-call limit (an atomic value, see mla_decode_set_small_call_limit).  Every
+ *     other entry point touches only the caller's buffers.
  */
 #ifndef MLA_DECODE_H_
 #define MLA_DECODE_H_
@@ -128,8 +129,11 @@ mla_status_t mla_decode_workspace_size(int B, int q_len, int H, int num_splits, 
  *   stream      the CUDA stream everything is enqueued on.
  *
  * Enqueues two kernels: the decode, and the split-K reduce (which waits for the decode by
- * programmatic dependent launch and also writes the status word).  No memset, no host
- * synchronisation.  Host-detected errors return before anything is enqueued.
+ * programmatic dependent launch and also writes the status word).  The decode is the
+ * tensor-core kernel, or, for a small bf16 call (see mla_decode_set_small_call_limit), a
+ * CUDA-core kernel with the same results contract; with num_splits == 0 that kernel keeps
+ * each (b, i) in one range.  No memset, no host synchronisation.  Host-detected errors
+ * return before anything is enqueued.
  */
 mla_status_t mla_decode(const void *q_nope, const void *q_pe, const void *kv_cache,
                         const int32_t *block_table, int max_pages, const int32_t *seq_lens,
@@ -161,6 +165,20 @@ mla_status_t mla_decode_ex(const void *q_nope, const void *q_pe, const void *kv_
                            int kv_dtype, float kv_scale, int num_splits, int window,
                            const float *sinks, void *workspace, size_t workspace_bytes, void *out,
                            float *lse, mla_stream_t stream);
+
+/*
+ * Small calls.  A bf16 call whose key ranges span at most `limit` cache positions each
+ * (max_pages*page_size; with num_splits > 0, roundup(cdiv(max_pages*page_size,
+ * num_splits), 64)), and whose (b, i, range, head) CTAs fit in one wave (at most the SM
+ * count), runs its decode on the CUDA cores: the tensor-core kernel's pipeline set-up
+ * (~9 us before its first P.V) is longer than such a call's whole work.  Results: as the tensor-core
+ * kernel's, to rounding (fp32 throughout, P not rounded to bf16); the forced-split
+ * partials and the plan in the workspace follow the same layout.  Sets the limit (0:
+ * never) for the calls enqueued after it returns, from any thread; returns the previous
+ * limit.  Default: MLA_SMALL_CALL_DEFAULT positions.
+ */
+#define MLA_SMALL_CALL_DEFAULT 256u
+size_t mla_decode_set_small_call_limit(size_t limit);
 
 /*
  * The split-K combine on its own (TileGym splitk_reduce): for every (b, i) whose KV range

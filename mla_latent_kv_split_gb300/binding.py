@@ -17,6 +17,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "lib", "libmla_decode.so")
 
 MLA_KV_BF16, MLA_KV_FP8_E4M3, MLA_KV_NVFP4 = 0, 1, 2
+MLA_SMALL_CALL_DEFAULT = 256  # include/mla_decode.h
 KV_DTYPE = {"bf16": MLA_KV_BF16, "fp8": MLA_KV_FP8_E4M3, "nvfp4": MLA_KV_NVFP4}
 STATUS_BITS = {
     0x1: "PAGE_OUT_OF_RANGE", 0x2: "SEQ_TOO_LONG", 0x4: "SEQ_LT_QLEN", 0x8: "NEG_SEQ_LEN",
@@ -26,6 +27,7 @@ EXPORTED = (
     "mla_decode_abi_version", "mla_status_string", "mla_decode_workspace_size", "mla_decode",
     "mla_splitk_reduce", "mla_decode_read_status", "mla_decode_num_workers", "mla_decode_plan_host",
     "mla_decode_no_alloc", "mla_decode_ex", "mla_kv_append", "mla_batched_gemv",
+    "mla_decode_set_small_call_limit",
 )
 
 
@@ -72,6 +74,8 @@ def lib() -> ctypes.CDLL:
             h.mla_kv_append.argtypes = [P, L64, P, L64, P, I, P, I, I, I, F, P, P]
             h.mla_batched_gemv.restype = I
             h.mla_batched_gemv.argtypes = [P, L64, L64, P, P, L64, L64, I, I, I, I, P, P]
+            h.mla_decode_set_small_call_limit.restype = Z
+            h.mla_decode_set_small_call_limit.argtypes = [Z]
             h.mla_decode_no_alloc.restype = I
             h.mla_decode_no_alloc.argtypes = [P, P, P, P, I, P, I, I, I, I, I, F, I, F, I, P, P, P,
                                               ctypes.POINTER(P)]
@@ -105,6 +109,12 @@ def mla_decode_workspace_size(B: int, q_len: int, H: int, num_splits: int = 0) -
     n = ctypes.c_size_t(0)
     _check("mla_decode_workspace_size", lib().mla_decode_workspace_size(B, q_len, H, num_splits, ctypes.byref(n)))
     return n.value
+
+
+def mla_decode_set_small_call_limit(limit: int) -> int:
+    """Sets the small-call limit (bf16 calls whose key ranges span at most this many cache
+    positions run on the CUDA-core decode kernel; 0: never); returns the previous limit."""
+    return int(lib().mla_decode_set_small_call_limit(int(limit)))
 
 
 def mla_decode_num_workers() -> int:

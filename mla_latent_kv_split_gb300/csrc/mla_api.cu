@@ -7,6 +7,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -16,6 +17,7 @@
 
 namespace mla {
 cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_decode_small(const DecodeParams& p, int parts_max, cudaStream_t stream);
 int tc_max_clusters();
 cudaError_t launch_splitk_reduce(uint8_t* ws, int U, int H, int slots_cap, int status_ctas, const float* sinks,
                                  uint16_t* out, float* lse, cudaStream_t stream, bool pdl);
@@ -86,9 +88,31 @@ int slots_that_fit(size_t workspace_bytes, int H) {
   return n > 0x7fffffff ? 0x7fffffff : (int)n;
 }
 
+// bf16 calls whose ranges span at most this many cache positions run on the CUDA-core
+// kernel; see mla_decode_set_small_call_limit.
+std::atomic<size_t> g_small_call_limit{MLA_SMALL_CALL_DEFAULT};
+
+// CTAs of the CUDA-core kernel for this call, or 0 when it goes to the tensor-core kernel.
+// A range's positions are bounded by the table's capacity (one range per (b, i)), or with
+// forced splits by the span of one part: roundup(cdiv(capacity, num_splits), 64).  The
+// kernel's CTAs (one per range and head, one resident per SM) must fit in one wave: a
+// second wave costs more than the tensor-core kernel's set-up.
+int small_call_ctas(int kv_dtype, int U, int H, int max_pages, int page_size, int num_splits, int workers) {
+  if (kv_dtype != MLA_KV_BF16) return 0;
+  const size_t cap = (size_t)max_pages * page_size;
+  const size_t span = num_splits > 0 ? (cap + num_splits - 1) / num_splits : cap;
+  if (((span + 63) & ~(size_t)63) > g_small_call_limit.load(std::memory_order_relaxed)) return 0;
+  const size_t ctas = (size_t)U * (num_splits > 0 ? num_splits : 1) * H;
+  return ctas <= (size_t)2 * workers && ctas <= (size_t)mla::kMaxCtas ? (int)ctas : 0;
+}
+
 }  // namespace
 
-MLA_EXPORT int mla_decode_abi_version(void) { return 2; }
+MLA_EXPORT size_t mla_decode_set_small_call_limit(size_t limit) {
+  return g_small_call_limit.exchange(limit);
+}
+
+MLA_EXPORT int mla_decode_abi_version(void) { return 3; }
 
 MLA_EXPORT const char* mla_status_string(mla_status_t s) {
   switch (s) {
@@ -199,9 +223,12 @@ MLA_EXPORT mla_status_t mla_decode_ex(const void* q_nope, const void* q_pe, cons
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // No host-side reset: each decode CTA writes its status word at exit and the reduce (which
   // always runs, after the decode) folds them into the call's status word.
-  cudaError_t le = mla::launch_decode_tc(p, s);
+  const int small_ctas = small_call_ctas(kv_dtype, U, H, max_pages, page_size, num_splits, p.workers);
+  cudaError_t le = small_ctas > 0 ? mla::launch_decode_small(p, num_splits > 0 ? num_splits : 1, s)
+                                  : mla::launch_decode_tc(p, s);
   if (le != cudaSuccess) return MLA_ERR_CUDA;
-  if (mla::launch_splitk_reduce(p.ws, U, H, p.slots_cap, 2 * p.workers, sinks, p.out, lse, s, true) != cudaSuccess)
+  const int status_ctas = small_ctas > 0 ? small_ctas : 2 * p.workers;
+  if (mla::launch_splitk_reduce(p.ws, U, H, p.slots_cap, status_ctas, sinks, p.out, lse, s, true) != cudaSuccess)
     return MLA_ERR_CUDA;
   return MLA_OK;
 }

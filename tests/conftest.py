@@ -27,3 +27,23 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+@pytest.fixture(autouse=True)
+def _tensor_core_path_for_gpu_tests(request):
+    """GPU tests drive the tensor-core decode kernel at every size: small bf16 calls would
+    otherwise go to the CUDA-core kernel (tests/test_gpu_small_path.py covers that one and
+    sets the limit itself)."""
+    if request.node.get_closest_marker("gpu") is None:
+        yield
+        return
+    try:
+        from mla_latent_kv_split_gb300 import binding as mb
+        old = mb.mla_decode_set_small_call_limit(0)
+    except Exception:  # library not built yet: the test's own fixtures build it
+        yield
+        return
+    try:
+        yield
+    finally:
+        mb.mla_decode_set_small_call_limit(old)

@@ -2,6 +2,8 @@
 C ABI binding, and compare with the float64 oracle at the stated tolerance."""
 from __future__ import annotations
 
+import contextlib
+
 import numpy as np
 import torch
 
@@ -17,6 +19,16 @@ from mla_latent_kv_split_gb300 import binding as mb
 # themselves.  The bf16 output, bf16 P and bf16 split partials each round at 2^-9
 # relative, so a correct row sits near 0.3 % (measured max below 1 %).
 ATOL, RTOL, LSE_ATOL, REL_L2, ROW_REL_L2 = 1e-2, 1e-2, 1e-3, 5e-3, 2e-2
+
+
+@contextlib.contextmanager
+def small_call_limit(limit: int):
+    """Runs the block with the library's small-call limit set to `limit`."""
+    old = mb.mla_decode_set_small_call_limit(limit)
+    try:
+        yield
+    finally:
+        mb.mla_decode_set_small_call_limit(old)
 
 
 def ensure_built():

@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(L):
     for name in declared:
         assert hasattr(L, name), name
     assert set(mb.EXPORTED) <= set(declared)
-    assert L.mla_decode_abi_version() == 2
+    assert L.mla_decode_abi_version() == 3
     for code in range(6):
         assert L.mla_status_string(code).decode().startswith("MLA_")
 
@@ -280,3 +280,17 @@ def test_verify_batch_schedule_aligns_the_queries_of_a_request(L):
             for (b0, i0, a0, e0), (b1, i1, a1, e1) in zip(mine, theirs):
                 assert b0 == b1 and i0 == 0 and i1 == i
                 assert abs(a0 - a1) <= 1 and abs(e0 - e1) <= 1
+
+
+def test_small_call_limit_setter_and_default():
+    """The small-call limit is a plain value: the setter returns the previous one, and the
+    binding's default mirrors the header's."""
+    import re
+    hdr = open(os.path.join(ROOT, "include", "mla_decode.h")).read()
+    m = re.search(r"#define MLA_SMALL_CALL_DEFAULT (\d+)u", hdr)
+    assert m and int(m.group(1)) == mb.MLA_SMALL_CALL_DEFAULT
+    old = mb.mla_decode_set_small_call_limit(123)
+    try:
+        assert mb.mla_decode_set_small_call_limit(456) == 123
+    finally:
+        assert mb.mla_decode_set_small_call_limit(old) == 456
