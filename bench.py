@@ -399,10 +399,12 @@ def measure_config(name: str, dev, l2_flush, steps: int, warmup: int, cpu_second
     sampler.start()
     times_ms, status = time_calls(case, l2_flush, steps, warmup)
     clocks = sampler.stop()
-    # the same calls with the kernels' instructions resident (a 1-request, 256-token call of
-    # the same cache format on its own inputs after each flush): as in a decode loop, where
-    # the kernels run every layer; the timed call's data stays cold
-    tw = W.WORKLOADS["tiny_contig_bf16"].scaled(kv_dtype=w.kv_dtype, H=w.H, num_splits=0)
+    # the same calls with the kernels' instructions resident (a 1-request call of the same
+    # shape class on its own inputs after each flush, which takes the same decode kernel:
+    # at most 1024 positions, the workload's own length if shorter): as in a decode loop,
+    # where the kernels run every layer; the timed call's data stays cold
+    warm_len = min(w.seq_len, 1024) if w.seq_len else 1024
+    tw = w.scaled(B=1, seq_lens_override=(warm_len,))
     tiny = DecodeCase(tw, W.make_inputs(tw), dev)
     warm_ms, _ = time_calls(case, l2_flush, steps, 3, prewarm=tiny.call)
     del case, tiny
