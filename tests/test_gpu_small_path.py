@@ -157,3 +157,56 @@ def test_small_poisoned_tails_bad_pages_and_empty_requests():
         out, lse, status, _ = run_decode(inp, num_splits=0)
     assert status & 0x4
     assert_close(out, lse, *oracle_ref(inp), what="small empty/short")
+
+
+def test_small_call_captured_in_a_graph():
+    """The CUDA-core decode and the combine inside a CUDA graph: replays equal an eager call
+    bit for bit, also after the queries and sequence lengths change in place."""
+    import torch
+    from gpu_util import to_device
+    w = W.WORKLOADS["paged_bf16_ragged"].scaled(B=4, H=16, seq_lens_override=(100, 250, 7, 64))
+    inp = W.make_inputs(w)
+    dev = to_device(inp)
+    ws = mb.alloc_workspace(w.B, w.q_len, w.H, 2)
+
+    def call(out=None, lse=None, stream=None):
+        return mb.mla_decode(dev["q_nope"], dev["q_pe"], dev["cache"], dev["block_table"], dev["seq_lens"],
+                             w.sm_scale, w.kv_dtype, inp["kv_scale"], 2, page_size=w.page_size,
+                             num_pages=inp["num_pages"], workspace=ws, out=out, lse=lse, stream=stream)
+
+    with small_call_limit(BIG):
+        ref_out, ref_lse = call()
+        torch.cuda.synchronize()
+        ref_out, ref_lse = ref_out.clone(), ref_lse.clone()
+        assert _plan(ws, 4)[1, 0] == 2  # forced splits: the partials and the combine are used
+        out, lse = torch.empty_like(ref_out), torch.empty_like(ref_lse)
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                call(out, lse, side)
+        torch.cuda.current_stream().wait_stream(side)
+        for _ in range(3):
+            out.fill_(float("nan"))
+            lse.fill_(float("nan"))
+            graph.replay()
+            torch.cuda.synchronize()
+            assert mb.mla_decode_read_status(ws) == 0
+            assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+            assert torch.equal(lse.view(torch.int32), ref_lse.view(torch.int32))
+        g = torch.Generator().manual_seed(7)
+        dev["q_nope"].copy_(torch.randn(dev["q_nope"].shape, generator=g).to(torch.bfloat16))
+        new_lens = np.array([60, 200, 3, 64], dtype=np.int32)
+        dev["seq_lens"].copy_(torch.from_numpy(new_lens))
+        graph.replay()
+        torch.cuda.synchronize()
+        ref2_out, ref2_lse = call()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), ref2_out.view(torch.int16))
+        assert torch.equal(lse.view(torch.int32), ref2_lse.view(torch.int32))
+    inp2 = dict(inp)
+    inp2["q_nope"] = dev["q_nope"].cpu().view(torch.int16).numpy().view(np.uint16)
+    inp2["seq_lens"] = new_lens
+    assert_close(out.float().cpu().double().numpy(), lse.cpu().double().numpy(), *oracle_ref(inp2),
+                 what="small call, graph replay")
