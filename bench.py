@@ -137,10 +137,20 @@ class ClockSampler:
             return
         self.thread = threading.Thread(target=lambda: [self.lines.append(l) for l in self.proc.stdout], daemon=True)
         self.thread.start()
+        # the first sample arrives a few hundred ms after the query starts: wait for it, so
+        # that the sampler is live when the timed region begins
+        t_end = time.time() + 3.0
+        while not self.lines and time.time() < t_end and self.proc.poll() is None:
+            time.sleep(0.01)
 
     def stop(self):
         if self.proc is None:
             return dict(sm_mhz=None, sm_max_mhz=None, reasons=["nvidia-smi unavailable"], samples=0)
+        # a timed region shorter than the 50 ms interval may hold no sample: take the next
+        # one too, so that the record brackets the region
+        n0, t_end = len(self.lines), time.time() + 1.0
+        while len(self.lines) == n0 and time.time() < t_end and self.proc.poll() is None:
+            time.sleep(0.005)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)

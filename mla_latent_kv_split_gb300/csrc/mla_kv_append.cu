@@ -3,8 +3,12 @@
 // tokens' latent and rope go to their cache locations before the decode reads them; metrale
 // "kv_cache_mla.rs", mla_cache_assemble and the NVFP4 / FP8 page layouts).
 //
-// One thread per 16-value group: a token is 36 groups (32 latent, 4 rope), a block of 288
-// threads takes 8 tokens, so a warp reads 32 consecutive groups (1 KB) of one token.
+// One thread per 16-value group of two tokens: a token is 36 groups (32 latent, 4 rope), a
+// block of 288 threads takes 16 tokens (thread i: group i % 36 of tokens i / 36 and i / 36 + 8),
+// so a warp reads 32 consecutive groups (1 KB) of one token.  Both tokens' loads are issued
+// before either is converted: with the occupancy bound below (5 blocks per SM) more bytes are
+// in flight than with one token per thread at 7 blocks per SM, which is what the quantising
+// formats need (FP8 -5 %, NVFP4 -7 % at 65,536 tokens; bf16 equal).
 //   bf16 : the group's 32 bytes copied.
 //   FP8  : 16 E4M3 codes of x / kv_scale (fp32 quotient), one 16-byte store.
 //   NVFP4: scale s = E4M3(amax / 6), 16 E2M1 codes of x / value(s) packed two per byte
@@ -26,8 +30,10 @@ namespace mla {
 namespace {
 
 constexpr int kGroups = 36;                      // 16-value groups per 576-value token
-constexpr int kAppendTokens = 8;                 // tokens per block
-constexpr int kAppendThreads = kGroups * kAppendTokens;
+constexpr int kAppendRows = 8;                   // token rows per block (36 threads each)
+constexpr int kTokensPerThread = 2;              // tokens kAppendRows apart
+constexpr int kAppendTokens = kAppendRows * kTokensPerThread;  // tokens per block
+constexpr int kAppendThreads = kGroups * kAppendRows;
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
@@ -77,23 +83,9 @@ __device__ __forceinline__ float e4m3_value(uint32_t code) {
 
 }  // namespace
 
-__global__ void __launch_bounds__(kAppendThreads)
-mla_kv_append_kernel(const uint16_t* __restrict__ latent, long long latent_stride, const uint16_t* __restrict__ rope,
-                     long long rope_stride, const int64_t* __restrict__ slots, int T, uint8_t* __restrict__ cache,
-                     long long num_slots, int page_size, int kv_dtype, float kv_scale, uint32_t* status) {
-  const int t = blockIdx.x * kAppendTokens + threadIdx.x / kGroups;
-  const int g = threadIdx.x % kGroups;
-  if (t >= T) return;
-  const long long slot = __ldg(slots + t);
-  if (slot < 0) return;  // padding
-  if (slot >= num_slots) {
-    if (g == 0 && status != nullptr) atomicOr(status, MLA_STATUS_SLOT_OUT_OF_RANGE);
-    return;
-  }
-  const uint16_t* lat = latent + (size_t)t * latent_stride;
-  const uint16_t* rp = rope + (size_t)t * rope_stride;
-  const uint4* src = reinterpret_cast<const uint4*>(g < 32 ? lat + 16 * g : rp + 16 * (g - 32));
-  const uint4 a = __ldg(src), b = __ldg(src + 1);
+// Group g of one token (its 16 values: a, b) -> the token's cache location `slot`.
+__device__ __forceinline__ void append_group(uint4 a, uint4 b, long long slot, int g, uint8_t* __restrict__ cache,
+                                             int page_size, int kv_dtype, float kv_scale) {
   if (kv_dtype == MLA_KV_BF16) {
     uint4* dst = reinterpret_cast<uint4*>(cache + (size_t)slot * (MLA_CACHE_DIM * 2) + 32 * g);
     dst[0] = a;
@@ -136,6 +128,39 @@ mla_kv_append_kernel(const uint16_t* __restrict__ latent, long long latent_strid
   uint8_t* base = cache + (size_t)page * ((size_t)page_size * (MLA_CACHE_DIM / 2 + MLA_CACHE_DIM / 16));
   *reinterpret_cast<uint2*>(base + row * (MLA_CACHE_DIM / 2) + 8 * g) = make_uint2(d0, d1);
   base[(size_t)page_size * (MLA_CACHE_DIM / 2) + row * (MLA_CACHE_DIM / 16) + g] = (uint8_t)s_code;
+}
+
+
+__global__ void __launch_bounds__(kAppendThreads, 5)
+mla_kv_append_kernel(const uint16_t* __restrict__ latent, long long latent_stride, const uint16_t* __restrict__ rope,
+                     long long rope_stride, const int64_t* __restrict__ slots, int T, uint8_t* __restrict__ cache,
+                     long long num_slots, int page_size, int kv_dtype, float kv_scale, uint32_t* status) {
+  const int row = threadIdx.x / kGroups;
+  const int g = threadIdx.x % kGroups;
+  uint4 a[kTokensPerThread], b[kTokensPerThread];
+  long long slot[kTokensPerThread];
+#pragma unroll
+  for (int j = 0; j < kTokensPerThread; ++j) {
+    const int t = blockIdx.x * kAppendTokens + j * kAppendRows + row;
+    slot[j] = -1;  // past the end: nothing to write
+    if (t < T) {
+      slot[j] = __ldg(slots + t);
+      const uint16_t* lat = latent + (size_t)t * latent_stride;
+      const uint16_t* rp = rope + (size_t)t * rope_stride;
+      const uint4* src = reinterpret_cast<const uint4*>(g < 32 ? lat + 16 * g : rp + 16 * (g - 32));
+      a[j] = __ldg(src);
+      b[j] = __ldg(src + 1);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kTokensPerThread; ++j) {
+    if (slot[j] < 0) continue;  // padding
+    if (slot[j] >= num_slots) {
+      if (g == 0 && status != nullptr) atomicOr(status, MLA_STATUS_SLOT_OUT_OF_RANGE);
+      continue;
+    }
+    append_group(a[j], b[j], slot[j], g, cache, page_size, kv_dtype, kv_scale);
+  }
 }
 
 cudaError_t launch_kv_append(const uint16_t* latent, long long latent_stride, const uint16_t* rope,
