@@ -21,6 +21,7 @@
 #include <stdint.h>
 
 #include "mla_device.cuh"
+#include "mla_ptx.cuh"
 
 namespace mla {
 
@@ -86,6 +87,23 @@ mla_decode_small_kernel(const DecodeParams p, int parts_max) {
     const int span = p.num_splits > 0 ? forced_span_tiles(tiles, p.num_splits) : tiles;
     const int t0 = unit_tile0(vis, p.window), tmin = window_first(vis, p.window);
     const int tok_lo = (t0 + k * span) * kTile, tok_hi = min((t0 + min((k + 1) * span, tiles)) * kTile, vis);
+    const int shift = p.page_size == 32 ? 5 : 6;
+    const uint16_t* cache = reinterpret_cast<const uint16_t*>(p.cache);
+    // The item's cache rows, asked into L2 at once, one bulk prefetch per page (by one CTA of
+    // every 16 heads): the warps' four-row steps then find them there instead of each step
+    // (and, before the first, the query row's load) waiting on HBM.
+    if ((h & 15) == 0 && warp == 0) {
+      const int lo = max(tok_lo, tmin);
+      const int pg_first = lo >> shift, n_pages = lo < tok_hi ? ((tok_hi - 1) >> shift) - pg_first + 1 : 0;
+      for (int j = lane; j < n_pages; j += 32) {
+        const int pi = pg_first + j;
+        const int pg = __ldg(table + pi);
+        if (pg >= 0 && pg < p.num_pages) {
+          const int r0 = max(lo, pi << shift) - (pi << shift), r1 = min(tok_hi, (pi + 1) << shift) - (pi << shift);
+          ptx::bulk_prefetch_l2(cache + ((size_t)pg * p.page_size + r0) * kDim, (uint32_t)(r1 - r0) * kDim * 2);
+        }
+      }
+    }
 
     float qn[16], qp[8];
     {
@@ -106,8 +124,6 @@ mla_decode_small_kernel(const DecodeParams p, int parts_max) {
       }
     }
     const float scale_log2 = p.sm_scale * 1.4426950408889634f;
-    const int shift = p.page_size == 32 ? 5 : 6;
-    const uint16_t* cache = reinterpret_cast<const uint16_t*>(p.cache);
 
     // ---- this warp's tokens: groups of 4 rows, warp w taking groups w, w + 8, ...
     float m = -INFINITY, l = 0.f, acc[16];
