@@ -264,22 +264,34 @@ __device__ __forceinline__ int q_row_exponent(uint32_t m) {
 // 2^k as a float, k in [-126, 127].
 __device__ __forceinline__ float pow2f(int k) { return __uint_as_float((uint32_t)(k + 127) << 23); }
 
-// Four fp32 bit patterns -> three words holding their top 24 bits (sign, exponent, 15
-// mantissa bits): w0 = a.hi16 | b.hi16 << 16, w1 = c.hi16 | d.hi16 << 16, w2 = the third
-// bytes of a, b, c, d.  The receiver fills the dropped low byte with another byte of the
-// packet, so the value it gets differs from the sent one by less than 2^-15 relative.
+// Four fp32 bit patterns -> three words holding their top 24 bits in value order: w0 = the
+// upper three bytes of a and the second byte of b, w1 = b's top two bytes and c's second and
+// third, w2 = c's top byte and the upper three of d, so that each word draws on two values
+// (one byte permute each).  The receiver rebuilds each value with one permute (d is w2
+// itself), filling the dropped low byte with another byte of the packet: the value it gets
+// differs from the sent one by less than 2^-15 relative.
 __device__ __forceinline__ void pack24x4(uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t& w0, uint32_t& w1,
                                          uint32_t& w2) {
-  w0 = __byte_perm(a, b, 0x7632);
-  w1 = __byte_perm(c, d, 0x7632);
-  w2 = __byte_perm(__byte_perm(a, b, 0x0051), __byte_perm(c, d, 0x5100), 0x7610);
+  w0 = __byte_perm(a, b, 0x5321);
+  w1 = __byte_perm(b, c, 0x6532);
+  w2 = __byte_perm(c, d, 0x7653);
 }
 __device__ __forceinline__ void unpack24x4(uint32_t w0, uint32_t w1, uint32_t w2, float& a, float& b, float& c,
                                            float& d) {
-  a = __uint_as_float(__byte_perm(w0, w2, 0x1044));
-  b = __uint_as_float(__byte_perm(w0, w2, 0x3255));
-  c = __uint_as_float(__byte_perm(w1, w2, 0x1066));
-  d = __uint_as_float(__byte_perm(w1, w2, 0x3277));
+  a = __uint_as_float(__byte_perm(w0, w0, 0x2103));
+  b = __uint_as_float(__byte_perm(w0, w1, 0x5436));
+  c = __uint_as_float(__byte_perm(w1, w2, 0x4325));
+  d = __uint_as_float(w2);
+}
+
+// Waits for this thread's tensor-memory loads; r's registers count as written by the wait, so
+// that no use of a load's result can be scheduled before it.
+__device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
 }
 
 // Bounded spin until this row's reference-max chain holds tile `g`'s predecessor's entry.
@@ -1257,11 +1269,8 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
       uint8_t* const stg0 = last ? S.stage[0] + sw * 16384 : S.ostage[sw];
       uint4* const part = reinterpret_cast<uint4*>(p.ws + partial_o_offset()) + (size_t)it.slot * 64 * p.H + row;
       const uint64_t pol_keep = ptx::l2_policy_evict_last();  // read again by the combine
-#pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
-        uint32_t r[16];
-        ptx::tmem_ld16(t_o + 128 * wg + 16 * c, r);
-        ptx::tmem_ld_wait();
+      // one 16-column chunk of this warpgroup's O, already in registers, scaled and stored
+      auto store_chunk = [&](int c, const uint32_t (&r)[16]) {
         if (!direct) {
           if (partial && real) {
             const int oct0 = (256 * (int)cr + 128 * wg + 16 * c) >> 3;
@@ -1275,7 +1284,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
                              ptx::pack_bf16x2(__uint_as_float(r[8 * k + 6]) * oscale, __uint_as_float(r[8 * k + 7]) * oscale)),
                   pol_keep);
           }
-          continue;
+          return;
         }
         uint8_t* const stg = last ? stg0 + 2048 * c : stg0;
         const uint32_t stg_a = ptx::smem_u32(stg);
@@ -1301,6 +1310,20 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
             if (32 * q + 16 * h < p.H) ptx::tma_store_2d(&tm_out, stg_a + h * 512, x, row0 + 16 * h);
           ptx::bulk_commit();
         }
+            };
+      // Chunks two at a time: chunk c + 1's tensor-memory load is in flight while chunk c is
+      // stored (the waits take the loaded registers as operands, so no use of a chunk can be
+      // scheduled before its wait).
+      uint32_t ra[16], rb[16];
+      ptx::tmem_ld16(t_o + 128 * wg, ra);
+#pragma unroll 1
+      for (int c = 0; c < 8; c += 2) {
+        tmem_ld_wait_regs(ra);
+        ptx::tmem_ld16(t_o + 128 * wg + 16 * (c + 1), rb);
+        store_chunk(c, ra);
+        tmem_ld_wait_regs(rb);
+        if (c + 2 < 8) ptx::tmem_ld16(t_o + 128 * wg + 16 * (c + 2), ra);
+        store_chunk(c + 1, rb);
       }
       if (real && cr == 0 && wg == 0) {
         if (direct) {
