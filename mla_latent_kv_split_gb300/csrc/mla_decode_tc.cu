@@ -943,11 +943,8 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
           dead = got < 0;
           break;
         }
+        // (an abort elsewhere reaches this loop through its bounded waits, which watch the flag)
         for (int t0 = it.tok_lo; t0 < it.tok_hi; t0 += kTileN, ++g) {
-          if (*abort_flag) {
-            dead = true;
-            break;
-          }
           if (decode_in_senders<KV>() && !prepare_tile<KV, kSenderThreads>(S, p, g, tq, cr, b_kv_full, b_kv_ready, 3, abort_flag)) {
             dead = true;
             break;
@@ -1088,6 +1085,14 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
           }
         }
         if (dead) break;
+        // ---- the tile's row mask (tail tiles only use it).  The producer published it with the
+        // tile's kv_full phase, which completed before this tile's scores (and cannot move on
+        // before P(gg) is handed over); it is read before the wait for the peer's scores, which
+        // usually takes longer.
+        const int st = real ? gg % kStages : 0;
+        if (real && !ptx::mbar_wait(b_kv_full + 8 * st, (gg / kStages) & 1, abort_flag)) { dead = true; break; }
+        const uint64_t full = kCols == 64 ? ~0ull : (1ull << kCols) - 1;
+        const uint64_t mask = (S.tmask[st] >> c0) & full;
         // ---- the peer's partial scores of this thread's columns (then the slot's next use is
         // armed: the peer pushes into it only after this tile's P.V, which every thread here
         // reaches only after this wait)
@@ -1115,14 +1120,7 @@ mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_co
           s[4 * j + 2] += c;
           s[4 * j + 3] += d;
         }
-        // ---- mask (tail tiles only), row max over this thread's columns (raw units; the
-        // scale is positive).  The producer published the tile's row mask with the tile's
-        // kv_full phase, which completed before this tile's scores (and cannot move on before
-        // P(gg) is handed over).
-        const int st = real ? gg % kStages : 0;
-        if (real && !ptx::mbar_wait(b_kv_full + 8 * st, (gg / kStages) & 1, abort_flag)) { dead = true; break; }
-        const uint64_t full = kCols == 64 ? ~0ull : (1ull << kCols) - 1;
-        const uint64_t mask = (S.tmask[st] >> c0) & full;
+        // ---- mask, row max over this thread's columns (raw units; the scale is positive)
         if (mask != full) {
 #pragma unroll
           for (int c = 0; c < kCols; ++c) s[c] = ((mask >> c) & 1ull) ? s[c] : -INFINITY;
