@@ -42,7 +42,7 @@ def _deps():
 # up after 20 ms instead of 4 s (and a waiting warp sleeps at most 0.1 ms at a time), and the exported mla_fault_injection_drop_tile makes one
 # CTA leave one tile unloaded, so that tests can run the kernel's abort path.
 FAULT_LIB = os.path.join(LIBDIR, "libmla_decode_fault_injection.so")
-FAULT_FLAGS = ("-DMLA_FAULT_INJECTION", "-DMLA_WAIT_LIMIT_NS=20000000ull", "-DMLA_SUSPEND_HINT_NS=100000u")
+FAULT_FLAGS = ("-DMLA_FAULT_INJECTION", "-DMLA_WAIT_LIMIT_NS=20000000ull")
 
 
 def up_to_date(lib: str = LIB) -> bool:

@@ -20,14 +20,10 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // ------------------------------------------------------------------ mbarrier
-// try_wait may suspend the waiting warp for up to this long; it resumes as soon as the phase
-// completes.  Suspension keeps waiting warps from flooding the shared-memory pipe with polls.
-// (A phase that never completes is noticed after 64 such suspensions at most; the test
-// build with short wait limits shortens the hint with them.)
-#ifndef MLA_SUSPEND_HINT_NS
-#define MLA_SUSPEND_HINT_NS 10000000u
-#endif
-constexpr uint32_t kSuspendHintNs = MLA_SUSPEND_HINT_NS;
+// try_wait without a time hint: the hardware may suspend the waiting warp for a short,
+// implementation-defined time and resumes it when the phase completes.  (An explicit hint,
+// from 100 ns to 10 ms, made every wait of the decode's per-tile chain slower: the kernel
+// took 1-2 % longer on every cache format.)
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
@@ -53,10 +49,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.b32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
+      : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
 }
@@ -77,10 +73,10 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.b32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
+      : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
 }
