@@ -45,7 +45,7 @@ mla_splitk_reduce_kernel(uint8_t* __restrict__ ws, int U, int H, int slots_cap, 
   }
   const int u = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int h = blockIdx.y * kReduceHeads + lane;
-  const int col0 = 128 * blockIdx.z + 16 * warp;  // this thread's 16 output columns
+  const int col0 = 16 * kReduceColGroups * blockIdx.z + 16 * warp;  // this thread's 16 output columns
   if (h >= H) return;
   const int2 pl = reinterpret_cast<const int2*>(ws + kPlanOffset)[u];
   const int parts = pl.x, slot = pl.y;
