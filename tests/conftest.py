@@ -14,7 +14,7 @@ def pytest_configure(config):
 
 
 def pytest_collection_modifyitems(config, items):
-    # GPU tests are skipped (not failed) when no GPU is visible; on a GPU machine the
+    # GPU tests are skipped (not failed) when no GPU is visible; on a machine with one the
     # library must load, and a missing library is a test failure.
     try:
         import torch
