@@ -139,6 +139,19 @@ def test_plan_heuristic_covers_and_balances(L, C):
         _check_plan(seq, q_len, 64, 0, C)
 
 
+@pytest.mark.parametrize("C", [76, 74, 64, 7])
+def test_plan_on_the_full_size_workloads(L, C):
+    """The schedule of every workload at its full size (the request lengths the bench and the
+    full-size parity tests use, drawn without the caches), checked by brute force with the
+    GB300's 76 workers and other worker counts (coverage, balance, contiguous partial slots,
+    at most 2C of them: the bound the heuristic-mode workspace is sized for)."""
+    import torch
+    from mla_latent_kv_split_gb300 import workloads as W
+    for w in W.WORKLOADS.values():
+        seq = W.draw_seq_lens(w, torch.Generator().manual_seed(w.seed))
+        _check_plan(seq, w.q_len, w.page_size, w.num_splits, C)
+
+
 @pytest.mark.parametrize("n", [1, 2, 3, 7])
 def test_plan_forced_splits(L, n):
     _check_plan([256, 1, 0, 700, 64, 65], 1, 64, n, 76)
