@@ -41,3 +41,23 @@ def test_code_hash_ignores_comments_only():
     assert bench._code_tokens(a) == bench._code_tokens(b)
     assert bench._code_tokens(a) != bench._code_tokens(c)
     assert len(bench.kernel_source_sha()) == 16
+
+
+def test_roofline_takes_the_binding_resource_of_each_format():
+    """bf16 at q_len 1 does 2*128*(576+512) flops per 1152 cache bytes (242 flops/byte), under
+    the ridge of the measured peaks, so it is HBM-bound; FP8 (576 bytes per token) and NVFP4
+    verify (324 bytes per token, four queries) are tensor-bound.  The fraction is the achieved
+    rate over the peak of that bound, and the roofline time the larger of the two times."""
+    peaks = {"hbm": 6775.3, "bf16": 1933.3, "source": "measured"}
+    tokens, H = 131072, 128
+    per_token_flops = 2.0 * H * (576 + 512)
+    for bpt, q_len, bound in ((1152, 1, "hbm"), (576, 1, "tensor"), (324, 4, "tensor")):
+        nbytes, flops = tokens * bpt, tokens * q_len * per_token_flops
+        t_mem, t_mma = nbytes / (peaks["hbm"] * 1e9), flops / (peaks["bf16"] * 1e12)
+        t = 2.5 * max(t_mem, t_mma)
+        roof = bench._roofline(nbytes, flops, t, peaks)
+        assert roof["bound"] == bound
+        assert roof["unit"] == ("GB/s" if bound == "hbm" else "TFLOP/s")
+        assert abs(roof["frac"] - 0.4) < 1e-12
+        assert abs(roof["roofline_us"] - 1e6 * max(t_mem, t_mma)) < 1e-9
+        assert roof["peak"] == (peaks["hbm"] if bound == "hbm" else peaks["bf16"])
